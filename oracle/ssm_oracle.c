@@ -1,0 +1,309 @@
+/*
+ * ssm_oracle.c -- serial fp64 reference for the forward selective scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  It shares no source,
+ * header, table or helper with the CUDA library; the two are independent
+ * statements of the same mathematics so that one can check the other.
+ *
+ * Sources (cited below by tag and section):
+ *   [P1] "Mamba hardware-aware parallel associative scan" (pwwt.cn/news/6375169)
+ *        sect. 1.2 (affine pair, composition, identity, discretisation),
+ *        sect. 2.1 (prefix result, Hillis-Steele, Blelloch, identity padding),
+ *        sect. 2.2 + 3.3 (chunked two-pass scan, boundary-state formula),
+ *        sect. 4.3 (numerics).
+ *   [P3] "Mamba (part 2): parallel scan and hardware-aware optimisation"
+ *        (scwacadex.pages.dev, blog8_mamba_parallel_scan)
+ *        sect. 2.1-2.3 (operator (x), associativity proof),
+ *        sect. 2.4 (tree reduction), sect. 4.3 (chunk-boundary states).
+ *
+ * Everything is computed in IEEE double with the plain definitions; nothing
+ * is blocked, fused or reordered beyond what the cited definition states.
+ * Inputs are read as float (the exact values the GPU receives: bf16 inputs
+ * are widened exactly to float by the caller) and widened to double here.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* Algebra of affine steps h -> a*h + b                                */
+/* ------------------------------------------------------------------ */
+
+/* [P1 sect. 1.2], [P3 sect. 2.2]: (a2,b2) o (a1,b1) = (a2*a1, a2*b1 + b2);
+ * the step on the left is applied after the step on the right. */
+void ssm_oracle_compose(double a2, double b2, double a1, double b1,
+                        double *a_out, double *b_out)
+{
+    *a_out = a2 * a1;
+    *b_out = a2 * b1 + b2;
+}
+
+/* [P1 sect. 2.1]: inclusive prefix (A_t, B_t) = (a_t,b_t) o ... o (a_1,b_1),
+ * so that h_t = A_t*h_0 + B_t.  Serial left-to-right evaluation. */
+void ssm_oracle_scan_serial(const double *a, const double *b, long L,
+                            double *A_out, double *B_out)
+{
+    double A = 1.0, B = 0.0;            /* identity (1,0) */
+    for (long t = 0; t < L; ++t) {
+        double nA, nB;
+        ssm_oracle_compose(a[t], b[t], A, B, &nA, &nB);
+        A = nA; B = nB;
+        A_out[t] = A; B_out[t] = B;
+    }
+}
+
+/* [P1 sect. 2.1] Hillis-Steele inclusive scan: ceil(log2 L) rounds; in round
+ * with distance d every i >= d takes (x[i]) o (x[i-d]).  Double buffered. */
+int ssm_oracle_scan_hillis_steele(const double *a, const double *b, long L,
+                                  double *A_out, double *B_out)
+{
+    if (L <= 0) return 0;
+    double *ta = (double *)malloc(sizeof(double) * (size_t)L);
+    double *tb = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!ta || !tb) { free(ta); free(tb); return -1; }
+    memcpy(A_out, a, sizeof(double) * (size_t)L);
+    memcpy(B_out, b, sizeof(double) * (size_t)L);
+    double *ca = A_out, *cb = B_out, *na = ta, *nb = tb;
+    for (long d = 1; d < L; d <<= 1) {
+        for (long i = 0; i < L; ++i) {
+            if (i >= d)
+                ssm_oracle_compose(ca[i], cb[i], ca[i - d], cb[i - d], &na[i], &nb[i]);
+            else { na[i] = ca[i]; nb[i] = cb[i]; }
+        }
+        double *s;
+        s = ca; ca = na; na = s;
+        s = cb; cb = nb; nb = s;
+    }
+    if (ca != A_out) {
+        memcpy(A_out, ca, sizeof(double) * (size_t)L);
+        memcpy(B_out, cb, sizeof(double) * (size_t)L);
+    }
+    free(ta); free(tb);
+    return 0;
+}
+
+/* [P1 sect. 2.1] Blelloch work-efficient scan.  The sequence is padded with
+ * the identity (1,0) up to a power of two, an up-sweep builds the reduction
+ * tree [P3 sect. 2.4], a down-sweep distributes exclusive prefixes, and the
+ * inclusive result is each element composed after its exclusive prefix. */
+int ssm_oracle_scan_blelloch(const double *a, const double *b, long L,
+                             double *A_out, double *B_out)
+{
+    if (L <= 0) return 0;
+    long P = 1;
+    while (P < L) P <<= 1;
+    double *ta = (double *)malloc(sizeof(double) * (size_t)P);
+    double *tb = (double *)malloc(sizeof(double) * (size_t)P);
+    if (!ta || !tb) { free(ta); free(tb); return -1; }
+    for (long i = 0; i < P; ++i) {
+        ta[i] = (i < L) ? a[i] : 1.0;
+        tb[i] = (i < L) ? b[i] : 0.0;
+    }
+    /* up-sweep: node at i+2d-1 becomes (right) o (left) */
+    for (long d = 1; d < P; d <<= 1) {
+        for (long i = 0; i < P; i += 2 * d) {
+            long l = i + d - 1, r = i + 2 * d - 1;
+            double na, nb;
+            ssm_oracle_compose(ta[r], tb[r], ta[l], tb[l], &na, &nb);
+            ta[r] = na; tb[r] = nb;
+        }
+    }
+    /* down-sweep: root gets the identity; each node passes its prefix to its
+     * left child, and (own left subtree total) o (prefix) to its right child */
+    ta[P - 1] = 1.0; tb[P - 1] = 0.0;
+    for (long d = P >> 1; d >= 1; d >>= 1) {
+        for (long i = 0; i < P; i += 2 * d) {
+            long l = i + d - 1, r = i + 2 * d - 1;
+            double la = ta[l], lb = tb[l];   /* left subtree total */
+            double pa = ta[r], pb = tb[r];   /* prefix arriving at this node */
+            ta[l] = pa; tb[l] = pb;
+            double na, nb;
+            ssm_oracle_compose(la, lb, pa, pb, &na, &nb);
+            ta[r] = na; tb[r] = nb;
+        }
+    }
+    for (long i = 0; i < L; ++i)
+        ssm_oracle_compose(a[i], b[i], ta[i], tb[i], &A_out[i], &B_out[i]);
+    free(ta); free(tb);
+    return 0;
+}
+
+/* [P1 sect. 2.2, 3.3] chunked two-pass scan.  The sequence is cut into chunks
+ * of length `chunk`; each chunk is scanned locally from the identity, giving
+ * its total (A_tot^(k), B_tot^(k)); the chunk start states follow
+ *     h_init^(0) = h0,  h_init^(k) = A_tot^(k-1) * h_init^(k-1) + B_tot^(k-1),
+ * and the fix-up gives h_t = A_loc_t * h_init^(k) + B_loc_t.
+ * Writes h_t for every t (h_out[t] is the state after step t), and the state
+ * at the end of every chunk into boundary[k] (k = 0 .. ceil(L/chunk)-1).  */
+int ssm_oracle_scan_chunked(const double *a, const double *b, long L, long chunk,
+                            double h0, double *h_out, double *boundary)
+{
+    if (L <= 0) return 0;
+    if (chunk <= 0) return -1;
+    long K = (L + chunk - 1) / chunk;
+    double *Atot = (double *)malloc(sizeof(double) * (size_t)K);
+    double *Btot = (double *)malloc(sizeof(double) * (size_t)K);
+    double *Aloc = (double *)malloc(sizeof(double) * (size_t)L);
+    double *Bloc = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!Atot || !Btot || !Aloc || !Bloc) {
+        free(Atot); free(Btot); free(Aloc); free(Bloc); return -1;
+    }
+    /* pass 1: independent local scans, one per chunk */
+    for (long k = 0; k < K; ++k) {
+        long s = k * chunk, e = s + chunk < L ? s + chunk : L;
+        ssm_oracle_scan_serial(a + s, b + s, e - s, Aloc + s, Bloc + s);
+        Atot[k] = Aloc[e - 1];
+        Btot[k] = Bloc[e - 1];
+    }
+    /* carry across chunks, then fix-up */
+    double hinit = h0;
+    for (long k = 0; k < K; ++k) {
+        long s = k * chunk, e = s + chunk < L ? s + chunk : L;
+        for (long t = s; t < e; ++t)
+            h_out[t] = Aloc[t] * hinit + Bloc[t];
+        if (boundary) boundary[k] = h_out[e - 1];
+        hinit = Atot[k] * hinit + Btot[k];
+    }
+    free(Atot); free(Btot); free(Aloc); free(Bloc);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Discretisation and gate                                             */
+/* ------------------------------------------------------------------ */
+
+/* softplus(v) = log(1 + e^v) ([P1 sect. 1.2]: the step is made positive by a
+ * softplus).  For v > 0 the same value is written v + log(1 + e^-v) so that
+ * e^v cannot overflow; both forms are the same real function. */
+double ssm_oracle_softplus(double v)
+{
+    if (v > 0.0) return v + log1p(exp(-v));
+    return log1p(exp(v));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z) */
+double ssm_oracle_silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/* ------------------------------------------------------------------ */
+/* Forward selective scan, the plain definition                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * For every channel (b, d), with h[n] = 0 at the start:
+ *   v      = delta[b,d,t] + dt_bias[d]                  (dt_bias optional)
+ *   Delta  = softplus(v) if `softplus` else v
+ *   a_n    = exp(Delta * A[d,n]),  b_n = Delta * B[b,n,t] * x[b,d,t]
+ *                                                       ([P1 sect. 1.2])
+ *   h[n]   = a_n * h[n] + b_n                           ([P1 sect. 1], [P3 sect. 1])
+ *   y      = sum_n C[b,n,t] * h[n]  + D[d] * x[b,d,t]   (D optional)
+ *   y     *= silu(z[b,d,t])                             (z optional)
+ * and final_state[b,d,n] = h[n] after the last step.
+ *
+ * Layouts (row-major): x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L];
+ * A: [dim, dstate]; D, dt_bias: [dim].
+ *
+ * `chan` selects which channels (index b*dim + d) to evaluate; NULL means all
+ * channels in order.  y is written as [nchan, L] and final_state as
+ * [nchan, dstate] in the order of `chan`.  `nthreads` > 1 evaluates
+ * independent channels on that many OpenMP threads (each channel is still
+ * the same serial loop); 0 leaves the OpenMP default.
+ * Returns 0, or -1 on bad arguments.
+ */
+int ssm_oracle_fwd(const float *x, const float *delta, const float *A,
+                   const float *Bm, const float *Cm, const float *Dskip,
+                   const float *z, const float *dt_bias, int softplus,
+                   double *y, double *final_state,
+                   long batch, long dim, long dstate, long L,
+                   const long *chan, long nchan, int nthreads)
+{
+    if (!x || !delta || !A || !Bm || !Cm || !y) return -1;
+    if (batch <= 0 || dim <= 0 || dstate <= 0 || L < 0) return -1;
+    long nall = batch * dim;
+    if (!chan) nchan = nall;
+    if (nchan < 0) return -1;
+    for (long i = 0; chan && i < nchan; ++i)
+        if (chan[i] < 0 || chan[i] >= nall) return -1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < nchan; ++i) {
+        long c = chan ? chan[i] : i;
+        long bb = c / dim, d = c % dim;
+        double *h = (double *)calloc((size_t)dstate, sizeof(double));
+        if (!h) {
+#pragma omp atomic write
+            err = 1;
+            continue;
+        }
+        const float *xr = x + (size_t)c * (size_t)L;
+        const float *dr = delta + (size_t)c * (size_t)L;
+        const float *zr = z ? z + (size_t)c * (size_t)L : NULL;
+        const float *Br = Bm + (size_t)bb * (size_t)dstate * (size_t)L;
+        const float *Cr = Cm + (size_t)bb * (size_t)dstate * (size_t)L;
+        const float *Ar = A + (size_t)d * (size_t)dstate;
+        double bias = dt_bias ? (double)dt_bias[d] : 0.0;
+        double Dd = Dskip ? (double)Dskip[d] : 0.0;
+        double *yr = y + (size_t)i * (size_t)L;
+        for (long t = 0; t < L; ++t) {
+            double xt = (double)xr[t];
+            double v = (double)dr[t] + bias;
+            double Delta = softplus ? ssm_oracle_softplus(v) : v;
+            double acc = 0.0;
+            for (long n = 0; n < dstate; ++n) {
+                double an = exp(Delta * (double)Ar[n]);
+                double bn = Delta * (double)Br[(size_t)n * (size_t)L + (size_t)t] * xt;
+                h[n] = an * h[n] + bn;
+                acc += (double)Cr[(size_t)n * (size_t)L + (size_t)t] * h[n];
+            }
+            double yv = acc + Dd * xt;
+            if (zr) yv *= ssm_oracle_silu((double)zr[t]);
+            yr[t] = yv;
+        }
+        if (final_state)
+            for (long n = 0; n < dstate; ++n)
+                final_state[(size_t)i * (size_t)dstate + (size_t)n] = h[n];
+        free(h);
+    }
+    return err ? -1 : 0;
+}
+
+/* The per-step pairs (a_t, b_t) of one recurrence (b, d, n), t = 0..L-1, as
+ * defined in [P1 sect. 1.2]; used to feed the scan orderings above with the
+ * exact pairs the forward recurrence consumes. */
+int ssm_oracle_pairs(const float *x, const float *delta, const float *A,
+                     const float *Bm, const float *dt_bias, int softplus,
+                     long batch, long dim, long dstate, long L,
+                     long b, long d, long n, double *a_out, double *b_out)
+{
+    if (b < 0 || b >= batch || d < 0 || d >= dim || n < 0 || n >= dstate) return -1;
+    long c = b * dim + d;
+    for (long t = 0; t < L; ++t) {
+        double xt = (double)x[(size_t)c * (size_t)L + (size_t)t];
+        double v = (double)delta[(size_t)c * (size_t)L + (size_t)t] + (dt_bias ? (double)dt_bias[d] : 0.0);
+        double Delta = softplus ? ssm_oracle_softplus(v) : v;
+        a_out[t] = exp(Delta * (double)A[(size_t)d * (size_t)dstate + (size_t)n]);
+        b_out[t] = Delta * (double)Bm[((size_t)b * (size_t)dstate + (size_t)n) * (size_t)L + (size_t)t] * xt;
+    }
+    return 0;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int ssm_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
