@@ -1,0 +1,176 @@
+/*
+ * ssm_scan.h -- C ABI of the GB300 forward selective-scan library
+ * (libssmscan.so, sm_103a).
+ *
+ * Operation.  For every channel (b, d) of a Mamba-style selective state-space
+ * layer with diagonal A, the library evaluates
+ *
+ *     Delta_t = softplus(delta[b,d,t] + dt_bias[d])          (or without softplus)
+ *     a_t[n]  = exp(Delta_t * A[d,n]),   b_t[n] = Delta_t * B[b,n,t] * x[b,d,t]
+ *     h_t[n]  = a_t[n] * h_{t-1}[n] + b_t[n],  h_{-1} = 0
+ *     y[b,d,t] = (sum_n C[b,n,t] * h_t[n] + D[d] * x[b,d,t]) * silu(z[b,d,t])
+ *
+ * as an associative scan over the affine pairs (a, b) under
+ * (a2,b2) o (a1,b1) = (a2*a1, a2*b1 + b2), identity (1, 0).
+ * Sources: "Mamba hardware-aware parallel associative scan"
+ * (pwwt.cn/news/6375169) sect. 1.2 (pairs, composition, discretisation),
+ * sect. 2.1-2.2 (prefix scan, chunked two-pass), sect. 3.3 (chunk carry),
+ * sect. 4.1 (fusion); "Mamba (part 2): parallel scan and hardware-aware
+ * optimisation" (scwacadex.pages.dev) sect. 2.2-2.4 (operator, tree),
+ * sect. 4.1-4.2 (fusion, intermediate states never written to HBM).
+ *
+ * Layouts (all row-major and contiguous, element type `io_dtype` unless
+ * stated):
+ *   x, delta, z, y : [batch, dim, seqlen]
+ *   B, C           : [batch, dstate, seqlen]
+ *   A              : [dim, dstate]            float32
+ *   D, dt_bias     : [dim]                    float32
+ *   final_state    : [batch, dim, dstate]     float32  (h after the last step)
+ *
+ * Ownership.  Every pointer of the device entry points is a device pointer
+ * owned by the caller.  The library allocates no memory and keeps no
+ * pointer after a call returns.  Inputs are only read.  `y` and
+ * `final_state` must not overlap any input.  Calls are asynchronous on
+ * `stream` (a cudaStream_t; NULL means the legacy default stream).
+ *
+ * Errors.  Arguments are validated on the host before anything is launched;
+ * a failed check returns a negative ssm_status_t and launches nothing.  A
+ * launch failure reported by the CUDA runtime returns SSM_ERR_LAUNCH.
+ * Device-side faults are not expected for validated arguments; none of the
+ * kernels waits on another block.
+ *
+ * Precision.  All arithmetic (discretisation, exp, scan, contraction, gate)
+ * is float32 for both I/O types; the state is float32.  bf16 outputs are
+ * rounded to nearest even.  Results differ from an exact evaluation only by
+ * float32 rounding (the scan order changes the rounding, not the result).
+ */
+#ifndef SSM_SCAN_H_
+#define SSM_SCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of x, delta, z, B, C and y. */
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = -1,        /* a required pointer is NULL                       */
+    SSM_ERR_DIMS = -2,        /* a size is out of range (see each entry point)    */
+    SSM_ERR_ALIGN = -3,       /* a pointer is not aligned to its element size     */
+    SSM_ERR_DTYPE = -4,       /* io_dtype is not an ssm_dtype_t                   */
+    SSM_ERR_WORKSPACE = -5,   /* workspace missing, too small or misaligned       */
+    SSM_ERR_LAUNCH = -6,      /* the CUDA runtime rejected a launch or a copy     */
+    SSM_ERR_UNSUPPORTED = -8, /* the variant cannot run this shape                */
+    SSM_ERR_ALIAS = -9,       /* an output overlaps an input                      */
+    SSM_ERR_VARIANT = -10     /* unknown variant number                           */
+} ssm_status_t;
+
+/* Evaluation strategies; all compute the same function.
+ *  FUSED   : channel-parallel, time-serial.  Each thread keeps a few states of
+ *            one channel in registers and walks the sequence in staged tiles
+ *            ("Mamba hardware-aware parallel associative scan", sect. 2.2,
+ *            third approach).  No workspace.
+ *  CHUNKED : each warp scans a chunk of 32*k steps: every lane runs k steps
+ *            serially, a warp-shuffle Hillis-Steele scan combines the lanes'
+ *            (a, b) totals, and the state is carried from chunk to chunk
+ *            (sect. 2.1 hybrid, sect. 3.2 warp shuffle).  No workspace.
+ *  TWOPASS : the sequence is cut into chunks processed in parallel; pass 1
+ *            writes every chunk's total (A_k, B_k), a small scan over the
+ *            chunk totals gives each chunk's start state, and pass 2 re-runs
+ *            the fused scan from that state (sect. 2.2, 3.3).  Needs
+ *            workspace.
+ *  AUTO    : the library picks one from the shape (ssm_scan_select_variant). */
+typedef enum {
+    SSM_VARIANT_AUTO = 0,
+    SSM_VARIANT_FUSED = 1,
+    SSM_VARIANT_CHUNKED = 2,
+    SSM_VARIANT_TWOPASS = 3
+} ssm_variant_t;
+
+/* Library version, (major << 16) | minor. */
+int ssm_scan_version(void);
+
+/* Static description of a status code (never NULL). */
+const char *ssm_scan_status_string(int status);
+
+/* The variant AUTO resolves to for this shape (host only, no GPU needed).
+ * Returns an ssm_variant_t > 0, or a negative status for invalid sizes. */
+int ssm_scan_select_variant(int batch, int dim, int dstate, int64_t seqlen, int io_dtype);
+
+/* Device workspace, in bytes, that ssm_scan_fwd needs for `variant` (AUTO
+ * resolves first).  0 means the workspace pointer may be NULL.  Returns
+ * (size_t)-1 for invalid sizes. */
+size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen,
+                                   int io_dtype, int variant);
+
+/*
+ * Forward selective scan on device buffers (the hot path).
+ *
+ *   x, delta      required.  [batch, dim, seqlen], io_dtype.
+ *   A             required.  [dim, dstate] float32 (normally negative).
+ *   B, C          required.  [batch, dstate, seqlen], io_dtype.
+ *   D             optional (NULL: no skip term).  [dim] float32.
+ *   z             optional (NULL: no gate).  [batch, dim, seqlen], io_dtype.
+ *   dt_bias       optional (NULL: zero bias).  [dim] float32.
+ *   delta_softplus  nonzero: Delta = softplus(delta + dt_bias); zero: Delta = delta + dt_bias.
+ *   y             required output.  [batch, dim, seqlen], io_dtype.
+ *   final_state   optional output (NULL: not written).  [batch, dim, dstate] float32.
+ *   batch, dim    >= 0 (0 is an empty problem: nothing is launched).
+ *   dstate        1 .. 64.
+ *   seqlen        >= 0 (0: y is empty and final_state, if given, is set to 0).
+ *   io_dtype      SSM_F32 or SSM_BF16.
+ *   workspace     device scratch of at least ssm_scan_fwd_workspace_size()
+ *                 bytes, 256-byte aligned; may be NULL when that size is 0.
+ *   stream        cudaStream_t to launch on.
+ * Alignment: io_dtype pointers must be aligned to the element size, float32
+ * pointers to 4 bytes.  16-byte aligned rows (seqlen * element size a
+ * multiple of 16 and 16-byte aligned bases) take the vectorised path;
+ * anything else runs the element-wise load path on the GPU.
+ * Returns SSM_OK or a negative ssm_status_t.
+ */
+int ssm_scan_fwd(const void *x, const void *delta, const float *A, const void *B,
+                 const void *C, const float *D, const void *z, const float *dt_bias,
+                 int delta_softplus, void *y, float *final_state,
+                 int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Same as ssm_scan_fwd with an explicit ssm_variant_t. */
+int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const void *B,
+                         const void *C, const float *D, const void *z, const float *dt_bias,
+                         int delta_softplus, void *y, float *final_state,
+                         int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                         void *workspace, size_t workspace_bytes, void *stream, int variant);
+
+/* Device bytes that ssm_scan_fwd_host needs as `device_buffer`: room for the
+ * device copies of every input and output plus the variant's workspace,
+ * each 256-byte aligned.  Returns (size_t)-1 for invalid sizes. */
+size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seqlen,
+                                     int io_dtype, int has_D, int has_z, int has_dt_bias,
+                                     int has_final_state, int variant);
+
+/*
+ * Forward selective scan on HOST buffers: the end-to-end call.  Same
+ * arguments and layouts as ssm_scan_fwd, but every tensor pointer is a host
+ * pointer (page-locked memory gives the fastest copies).  The inputs are
+ * copied into `device_buffer` (caller-owned device memory of at least
+ * ssm_scan_fwd_host_buffer_size() bytes, 256-byte aligned) with one
+ * cudaMemcpyAsync each, the scan runs on `stream`, y and final_state are
+ * copied back, and the call returns after `stream` has finished them.
+ */
+int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const void *B,
+                      const void *C, const float *D, const void *z, const float *dt_bias,
+                      int delta_softplus, void *y, float *final_state,
+                      int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                      void *device_buffer, size_t device_buffer_bytes, void *stream,
+                      int variant);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H_ */

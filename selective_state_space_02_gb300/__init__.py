@@ -1,0 +1,161 @@
+"""GB300-native forward selective scan (Mamba-style SSM), sm_103a.
+
+Thin PyTorch binding over libssmscan.so (include/ssm_scan.h): it checks
+dtypes, devices and contiguity, allocates outputs with torch, and passes raw
+pointers and the current CUDA stream.  Every step of the scan runs in the
+library's kernels; there is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _native
+from ._native import ScanError, VARIANTS, SSM_BF16, SSM_F32
+
+__all__ = ["scan_fwd", "scan_fwd_host", "select_variant", "workspace_size", "ScanError",
+           "VARIANTS", "host_buffer_size"]
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return SSM_F32
+    if t == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported I/O dtype {t}; use float32 or bfloat16")
+
+
+def _variant_code(variant) -> int:
+    if isinstance(variant, str):
+        return VARIANTS[variant]
+    return int(variant)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def select_variant(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.float32) -> str:
+    v = _native.load().ssm_scan_select_variant(batch, dim, dstate, seqlen, _dtype_code(dtype))
+    if v < 0:
+        _native.check(v)
+    return _native.VARIANT_NAMES[v]
+
+
+def workspace_size(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.float32,
+                   variant="auto") -> int:
+    n = _native.load().ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen, _dtype_code(dtype),
+                                                   _variant_code(variant))
+    if n == (1 << 64) - 1:
+        raise ScanError(-2, "invalid sizes")
+    return n
+
+
+def host_buffer_size(batch, dim, dstate, seqlen, dtype, has_D, has_z, has_dt_bias,
+                     has_final_state, variant="auto") -> int:
+    n = _native.load().ssm_scan_fwd_host_buffer_size(batch, dim, dstate, seqlen, _dtype_code(dtype),
+                                                     int(has_D), int(has_z), int(has_dt_bias),
+                                                     int(has_final_state), _variant_code(variant))
+    if n == (1 << 64) - 1:
+        raise ScanError(-2, "invalid sizes")
+    return n
+
+
+def _check_inputs(x, delta, A, B, C, D, z, dt_bias, device_type):
+    io = x.dtype
+    _dtype_code(io)
+    ios = (("x", x), ("delta", delta), ("B", B), ("C", C), ("z", z))
+    f32s = (("A", A), ("D", D), ("dt_bias", dt_bias))
+    for name, t in ios:
+        if t is not None and t.dtype != io:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected {io}")
+    for name, t in f32s:
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    for name, t in ios + f32s:
+        if t is None:
+            continue
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.type != device_type:
+            raise ValueError(f"{name} must be on {device_type}")
+    if x.dim() != 3:
+        raise ValueError("x must be [batch, dim, seqlen]")
+    batch, dim, L = x.shape
+    N = A.shape[1]
+    if delta.shape != x.shape or (z is not None and z.shape != x.shape):
+        raise ValueError("delta and z must have the shape of x")
+    if A.shape != (dim, N) or B.shape != (batch, N, L) or C.shape != (batch, N, L):
+        raise ValueError("A must be [dim, dstate]; B and C [batch, dstate, seqlen]")
+    for name, t in (("D", D), ("dt_bias", dt_bias)):
+        if t is not None and t.shape != (dim,):
+            raise ValueError(f"{name} must be [dim]")
+    return batch, dim, N, L
+
+
+def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+             C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+             dt_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+             return_final_state: bool = False, variant="auto", y: Optional[torch.Tensor] = None,
+             final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Forward selective scan on CUDA tensors, launched on the current stream.
+
+    x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (float32 or
+    bfloat16, all the same); A: [dim, dstate], D, dt_bias: [dim] (float32).
+    Returns y (same dtype as x), or (y, final_state [batch, dim, dstate]
+    float32) when ``return_final_state``.  ``y``, ``final_state`` and
+    ``workspace`` may be given to avoid allocations.
+    """
+    batch, dim, N, L = _check_inputs(x, delta, A, B, C, D, z, dt_bias, "cuda")
+    lib = _native.load()
+    code = _dtype_code(x.dtype)
+    v = _variant_code(variant)
+    if y is None:
+        y = torch.empty_like(x)
+    if return_final_state and final_state is None:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=x.device)
+    ws_bytes = lib.ssm_scan_fwd_workspace_size(batch, dim, N, L, code, v)
+    if ws_bytes == (1 << 64) - 1:
+        raise ScanError(-2, "invalid sizes")
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    rc = lib.ssm_scan_fwd_variant(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                  _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y),
+                                  _ptr(final_state) if return_final_state else None,
+                                  batch, dim, N, L, code,
+                                  _ptr(workspace) if ws_bytes else None,
+                                  ws_bytes, stream, v)
+    _native.check(rc)
+    if return_final_state:
+        return y, final_state
+    return y
+
+
+def scan_fwd_host(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                  C: torch.Tensor, D=None, z=None, dt_bias=None, delta_softplus: bool = True,
+                  y: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                  device_buffer: Optional[torch.Tensor] = None, variant="auto", stream=None):
+    """End-to-end call on CPU tensors (pinned memory recommended): copies the
+    inputs to the GPU, runs the scan and copies y (and final_state, if a
+    tensor is given) back before returning.  ``device_buffer`` is a CUDA
+    uint8 tensor of at least ``host_buffer_size(...)`` bytes."""
+    batch, dim, N, L = _check_inputs(x, delta, A, B, C, D, z, dt_bias, "cpu")
+    lib = _native.load()
+    code = _dtype_code(x.dtype)
+    v = _variant_code(variant)
+    if y is None:
+        y = torch.empty_like(x)
+    need = lib.ssm_scan_fwd_host_buffer_size(batch, dim, N, L, code, int(D is not None),
+                                             int(z is not None), int(dt_bias is not None),
+                                             int(final_state is not None), v)
+    if device_buffer is None or device_buffer.numel() < need:
+        device_buffer = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    rc = lib.ssm_scan_fwd_host(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                               _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), _ptr(final_state),
+                               batch, dim, N, L, code, _ptr(device_buffer), need, stream.cuda_stream, v)
+    _native.check(rc)
+    return y

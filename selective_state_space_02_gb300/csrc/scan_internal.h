@@ -1,0 +1,41 @@
+// Internal interface between the C ABI (ssm_scan_api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/ssm_scan.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ssm {
+
+// One validated forward problem (all pointers are device pointers).
+struct FwdArgs {
+    const void *x;
+    const void *delta;
+    const float *A;
+    const void *B;
+    const void *C;
+    const float *D;        // nullable
+    const void *z;         // nullable
+    const float *dt_bias;  // nullable
+    int softplus;
+    void *y;
+    float *final_state;    // nullable
+    int batch;
+    int dim;
+    int dstate;
+    int64_t L;
+    int bf16;              // 1: io elements are bf16, 0: float32
+    int vec16;             // 1: every io row starts 16-byte aligned
+};
+
+// Each launcher returns cudaSuccess or the launch error.
+cudaError_t launch_fused(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_chunked(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t s);
+
+// Chunk length and workspace bytes of the two-pass variant.
+int64_t twopass_chunk_len(int batch, int dim, int dstate, int64_t L);
+size_t twopass_workspace_bytes(int batch, int dim, int dstate, int64_t L);
+
+}  // namespace ssm

@@ -1,0 +1,160 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before launching
+anything (every call below fails validation, so no kernel is launched and
+no fake pointer is ever dereferenced)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import selective_state_space_02_gb300 as ssm
+from selective_state_space_02_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+OK, ERR_NULL, ERR_DIMS, ERR_ALIGN, ERR_DTYPE, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+ERR_ALIAS, ERR_VARIANT = -9, -10
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _native.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(ssm_[a-z_0-9]+)\s*\(", src, re.M)))
+
+
+def test_header_declares_entry_points():
+    names = _declared_functions()
+    assert "ssm_scan_fwd" in names and "ssm_scan_fwd_host" in names
+    assert set(names) == set(_native.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_no_torch_in_the_abi():
+    src = open(HEADER).read()
+    assert "torch" not in src.lower().replace("pytorch", "") and "at::" not in src
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ssm_scan_version() >> 16 == 1
+    for s in (OK, ERR_NULL, ERR_DIMS, ERR_ALIGN, ERR_DTYPE, ERR_WORKSPACE, -6, -8, ERR_ALIAS, ERR_VARIANT, 12345):
+        assert isinstance(_native.status_string(s), str) and _native.status_string(s)
+
+
+def test_variant_selection_host_only(lib):
+    assert ssm.select_variant(4, 1536, 16, 2048) == "fused"
+    assert ssm.select_variant(8, 2048, 16, 4096) == "fused"
+    assert ssm.select_variant(2, 5120, 64, 8192) == "fused"
+    assert ssm.select_variant(1, 768, 16, 131072) == "chunked"
+    assert ssm.select_variant(1, 64, 16, 1 << 20) == "twopass"
+    assert lib.ssm_scan_select_variant(1, 1, 0, 10, 0) == ERR_DIMS
+    assert lib.ssm_scan_select_variant(1, 1, 65, 10, 0) == ERR_DIMS
+    assert lib.ssm_scan_select_variant(1, 1, 16, 10, 3) == ERR_DTYPE
+
+
+def test_workspace_sizes(lib):
+    for v in ("fused", "chunked"):
+        assert ssm.workspace_size(4, 1536, 16, 2048, variant=v) == 0
+    assert ssm.workspace_size(1, 64, 16, 0, variant="twopass") == 0
+    assert lib.ssm_scan_fwd_workspace_size(1, 1, 99, 10, 0, 0) == (1 << 64) - 1
+    assert lib.ssm_scan_fwd_workspace_size(1, 1, 16, 10, 0, 7) == (1 << 64) - 1
+
+
+def test_twopass_workspace_matches_chunk_state_ledger(lib):
+    """The two-pass workspace holds one (batch, dim, dstate) fp32 state per
+    chunk plus one sum of Delta per (batch, dim) and chunk.  The scan page's
+    memory ledger (sect. 3.4) prints the per-chunk state of its example."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "ledger.json")))
+    sh, pr = g["shape"], g["printed"]
+    per_chunk = sh["batch"] * sh["d_inner"] * sh["d_state"]
+    assert per_chunk == pr["elements_per_chunk_state"]
+    assert per_chunk * 4 / 2 ** 20 == pytest.approx(pr["mb_per_chunk_state_fp32"])
+    assert sh["seq_len"] // sh["chunk"] == pr["chunks"]
+    assert round(pr["chunks"] * per_chunk * 4 / 1e6, 1) == pr["mb_all_chunk_states_fp32"]
+    full = per_chunk * sh["seq_len"]
+    assert float(f"{full:.2e}") == pr["elements_all_states"]
+    assert round(full * 4 / 1e9, 1) == pr["gb_all_states_fp32"]
+    # our workspace for that shape: K chunk states + K delta sums, 256-byte rounded
+    ws = ssm.workspace_size(sh["batch"], sh["d_inner"], sh["d_state"], sh["seq_len"], variant="twopass")
+    r256 = lambda n: (n + 255) // 256 * 256
+    ks = [k for k in range(1, 64) if r256(k * per_chunk * 4) + r256(k * sh["batch"] * sh["d_inner"] * 4) == ws]
+    assert len(ks) == 1, "workspace is not a whole number of chunk states"
+    assert ws < full * 4 / 100, "the workspace must stay far below the full state tensor"
+
+
+def _fwd(lib, x=8, delta=16 * 64, A=16 * 4096, B=16 * 8192, C=16 * 16384, D=None, z=None, dt=None,
+         sp=1, y=16 * 32768, fs=None, batch=1, dim=2, dstate=4, L=8, dtype=0, ws=None, wsb=0, stream=None,
+         variant=0):
+    # fake, well-separated, 16-byte aligned addresses: every case below must
+    # fail validation before any launch
+    x = 16 * 2 if x == 8 else x
+    return lib.ssm_scan_fwd_variant(x, delta, A, B, C, D, z, dt, sp, y, fs, batch, dim, dstate, L, dtype,
+                                    ws, wsb, stream, variant)
+
+
+def test_rejects_null_pointers(lib):
+    assert _fwd(lib, x=None) == ERR_NULL
+    assert _fwd(lib, delta=None) == ERR_NULL
+    assert _fwd(lib, A=None) == ERR_NULL
+    assert _fwd(lib, B=None) == ERR_NULL
+    assert _fwd(lib, C=None) == ERR_NULL
+    assert _fwd(lib, y=None) == ERR_NULL
+
+
+def test_rejects_bad_sizes_and_dtype(lib):
+    assert _fwd(lib, batch=-1) == ERR_DIMS
+    assert _fwd(lib, dim=-3) == ERR_DIMS
+    assert _fwd(lib, dstate=0) == ERR_DIMS
+    assert _fwd(lib, dstate=65) == ERR_DIMS
+    assert _fwd(lib, L=-1) == ERR_DIMS
+    assert _fwd(lib, dtype=2) == ERR_DTYPE
+
+
+def test_rejects_misaligned(lib):
+    assert _fwd(lib, x=16 * 2 + 2) == ERR_ALIGN           # f32 needs 4-byte alignment
+    assert _fwd(lib, A=16 * 4096 + 1) == ERR_ALIGN
+    assert _fwd(lib, y=16 * 32768 + 1, dtype=1) == ERR_ALIGN
+
+
+def test_rejects_aliasing(lib):
+    assert _fwd(lib, y=16 * 2) == ERR_ALIAS                # y == x
+    assert _fwd(lib, fs=16 * 4096) == ERR_ALIAS             # final state over A
+    assert _fwd(lib, fs=16 * 32768 + 4) == ERR_ALIAS        # final state inside y
+
+
+def test_rejects_missing_workspace_and_bad_variant(lib):
+    assert _fwd(lib, variant=3) == ERR_WORKSPACE
+    assert _fwd(lib, variant=3, ws=16 * 65536 + 16, wsb=1 << 20) == ERR_WORKSPACE   # not 256-aligned
+    assert _fwd(lib, variant=3, ws=16 * 65536, wsb=4) == ERR_WORKSPACE               # too small
+    assert _fwd(lib, variant=9) == ERR_VARIANT
+
+
+def test_empty_problems_launch_nothing(lib):
+    assert _fwd(lib, batch=0) == OK
+    assert _fwd(lib, dim=0) == OK
+    assert _fwd(lib, L=0) == OK                              # no final state requested
+
+
+def test_binding_type_checks():
+    import torch
+    x = torch.zeros(1, 2, 8)
+    A = torch.zeros(2, 4)
+    B = torch.zeros(1, 4, 8)
+    with pytest.raises(TypeError):
+        ssm.scan_fwd(x.double(), x.double(), A, B, B)
+    with pytest.raises(TypeError):
+        ssm.scan_fwd(x, x.bfloat16(), A, B, B)
+    with pytest.raises(ValueError):
+        ssm.scan_fwd(x, x, A, B, B)                          # CPU tensors on the device path
