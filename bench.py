@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the forward selective scan on GB300.
+
+One step = one call of the hot path (ssm_scan_fwd through the C ABI) over one
+batch of the synthetic workload, inputs resident in HBM.  Prints ONE JSON
+line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--variant auto|fused|chunked|twopass] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run, one rank per GPU: every rank scans its
+own batch of the same shape (weak scaling, no data-path collective); the
+elapsed time is the maximum over ranks.  ``--impl reference`` times the fp64
+CPU oracle (the deliberately slow reference arm) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan Gelem/s (B·D·L/s) and achieved HBM GB/s as % of GB300 roofline"
+UNIT = "Gelem/s"
+DEFAULT_WORKLOAD = "mid_bf16"
+SMS = 152                      # GB300 streaming multiprocessors
+SM_MAX_MHZ = 2070.0            # maximum SM clock
+UPDATES_PER_CLK_SM = 32        # (t,d,n) updates per clock per SM: 128 FP32 lanes / 4 ops, 32 ex2/clk
+HBM_FALLBACK_GBS = 6800.0
+KERNELS_PER_STEP = {"fused": 1, "chunked": 1, "twopass": 3}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.json")
+KERNEL_SOURCES = {
+    "fused": ["selective_state_space_02_gb300/csrc/scan_fused.cu"],
+    "twopass": ["selective_state_space_02_gb300/csrc/scan_fused.cu"],
+    "chunked": ["selective_state_space_02_gb300/csrc/scan_chunked.cu"],
+}
+
+
+# ----------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--variant", default="auto")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--flush-mib", type=int, default=512, help="L2 flush buffer written between timed steps")
+    ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clock sampling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    return a
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest `value` over all ranks (the job's elapsed time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank scans its own batch: same shape, different seeded data."""
+    return base_seed + 1000003 * rank
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def alu_peak_updates_per_s() -> float:
+    return SMS * SM_MAX_MHZ * 1e6 * UPDATES_PER_CLK_SM
+
+
+def source_hash(variant: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES.get(variant, []) + ["selective_state_space_02_gb300/csrc/scan_device.cuh"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, variant: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            j = json.load(f)
+        e = j[workload][variant]
+        if e.get("source_hash") != source_hash(variant):
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the GPU is busy."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(device_index)
+            self.pci = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+        except Exception:
+            self.pci = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.pci:
+            cmd += ["-i", self.pci]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        # wait for the first sample so the load phase is covered
+        deadline = time.time() + 3.0
+        while self.proc and time.time() < deadline and os.path.getsize(self.path) == 0:
+            time.sleep(0.05)
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "", 1).isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        pw = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows)}
+
+
+def workload_problem(name: str, rank: int):
+    from selective_state_space_02_gb300 import synth
+    cfg = dict(synth.WORKLOADS[name])
+    cfg["seed"] = rank_seed(cfg["seed"], rank)
+    return synth.make_problem(**cfg), cfg
+
+
+def cpu_baseline(p, max_seconds: float = 20.0):
+    """Time the fp64 oracle on the host cores over a bounded sample of the
+    workload (whole channels, every step)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    nch = p.batch * p.dim
+    arrs = dict(x=p.f32("x"), delta=p.f32("delta"), A=p.A.numpy(), B=p.f32("B"), C=p.f32("C"),
+                D=None if p.D is None else p.D.numpy(), z=p.f32("z"),
+                dt_bias=None if p.dt_bias is None else p.dt_bias.numpy())
+    threads = oracle.max_threads()
+    # calibrate on a few channels, then size the sample to ~max_seconds / 2
+    probe = list(range(min(nch, max(threads, 8))))
+    t = time.perf_counter()
+    oracle.fwd(arrs["x"], arrs["delta"], arrs["A"], arrs["B"], arrs["C"], arrs["D"], arrs["z"],
+               arrs["dt_bias"], p.delta_softplus, channels=probe, return_final_state=False)
+    per_chan = (time.perf_counter() - t) / len(probe)
+    k = int(min(nch, max(len(probe), (max_seconds / 2) / max(per_chan, 1e-9))))
+    chans = list(range(k)) if k == nch else sorted(np.random.default_rng(0).choice(nch, k, replace=False).tolist())
+    t = time.perf_counter()
+    oracle.fwd(arrs["x"], arrs["delta"], arrs["A"], arrs["B"], arrs["C"], arrs["D"], arrs["z"],
+               arrs["dt_bias"], p.delta_softplus, channels=chans, return_final_state=False)
+    dt = time.perf_counter() - t
+    elems = k * p.seqlen
+    sample = ("whole workload" if k == nch else f"{k} of {nch} channels") + \
+        f", all {p.seqlen} steps, one pass ({dt:.2f} s)"
+    return {"value": elems / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import selective_state_space_02_gb300 as ssm
+    from selective_state_space_02_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    p, cfg = workload_problem(args.workload, rank)
+    g = lambda t: None if t is None else t.to(dev)
+    x, dl, z, B, C, A, D, bias = (g(p.x), g(p.delta), g(p.z), g(p.B), g(p.C), g(p.A), g(p.D), g(p.dt_bias))
+    variant = args.variant if args.variant != "auto" else ssm.select_variant(
+        p.batch, p.dim, p.dstate, p.seqlen, p.torch_dtype)
+    y = torch.empty_like(x)
+    fs = torch.empty(p.batch, p.dim, p.dstate, device=dev) if p.final_state else None
+    wsb = ssm.workspace_size(p.batch, p.dim, p.dstate, p.seqlen, p.torch_dtype, variant)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssm.scan_fwd(x, dl, A, B, C, D=D, z=z, dt_bias=bias, delta_softplus=p.delta_softplus,
+                     return_final_state=fs is not None, variant=variant, y=y, final_state=fs, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.time() + args.soak_s
+    while time.time() < t_end:          # untimed load: clocks settle, sampler sees the load
+        for _ in range(20):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()                   # L2 flush, outside the timed events
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]     # ms per step (device)
+    total_ms = max_over_ranks(sum(per), world, dev)
+    ms_per_step = total_ms / args.steps
+    elems = p.elems
+    value = world * elems * args.steps / (total_ms / 1e3) / 1e9
+
+    hbm_peak, peak_kind = measured_peaks()
+    mb = synth.min_bytes(p)
+    kern_s = statistics.mean(per) / 1e3
+    hbm_gbs = mb / kern_s / 1e9
+    updates = elems * p.dstate
+    alu_achieved = updates / kern_s
+    alu_peak = alu_peak_updates_per_s()
+    traffic = profiled_traffic(args.workload, variant)
+    roofline = {
+        "bound": "alu",
+        "achieved": round(alu_achieved / 1e12, 4),
+        "peak": round(alu_peak / 1e12, 4),
+        "unit": "Tupdate/s",
+        "frac": round(alu_achieved / alu_peak, 4),
+        "traffic": traffic,
+        "kernel": f"{variant} scan",
+        "peak_basis": f"{SMS} SMs x {SM_MAX_MHZ:.0f} MHz x {UPDATES_PER_CLK_SM} (t,d,n) updates/clk/SM "
+                      "(1 ex2 + 4 FP32 ops per update; 32 ex2 and 128 FP32 lanes per clk per SM)",
+        "hbm": {"achieved": round(hbm_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(hbm_gbs / hbm_peak, 4), "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": mb},
+    }
+
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: None if t is None else t.pin_memory()
+        hx, hdl, hz, hB, hC, hA, hD, hb = (pin(p.x), pin(p.delta), pin(p.z), pin(p.B), pin(p.C), pin(p.A),
+                                           pin(p.D), pin(p.dt_bias))
+        hy = torch.empty_like(hx).pin_memory()
+        hfs = torch.empty(p.batch, p.dim, p.dstate).pin_memory() if p.final_state else None
+        need = ssm.host_buffer_size(p.batch, p.dim, p.dstate, p.seqlen, p.torch_dtype, hD is not None,
+                                    hz is not None, hb is not None, hfs is not None, variant)
+        dbuf = torch.empty(need, dtype=torch.uint8, device=dev)
+
+        def hstep():
+            ssm.scan_fwd_host(hx, hdl, hA, hB, hC, D=hD, z=hz, dt_bias=hb, delta_softplus=p.delta_softplus,
+                              y=hy, final_state=hfs, device_buffer=dbuf, variant=variant, stream=stream)
+
+        for _ in range(args.warmup):
+            hstep()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            hstep()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (hx, hdl, hz, hB, hC, hA, hD, hb) if t is not None)
+        d2h = hy.numel() * hy.element_size() + (hfs.numel() * 4 if hfs is not None else 0)
+        e2e = {"value": world * elems * args.steps / t_e2e / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "ssm_scan_fwd_host (pinned host buffers, copies inside the timed region)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(p)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": p.batch, "dim": p.dim, "dstate": p.dstate,
+                   "seqlen": p.seqlen, "io_dtype": p.dtype, "gate": p.z is not None,
+                   "final_state": p.final_state, "variant": variant,
+                   "l2": f"flushed between timed steps ({args.flush_mib} MiB write, outside the timed events)",
+                   "parallelism": f"{world} independent replicas, one batch each" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "gpu_launches": args.steps * KERNELS_PER_STEP[variant],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from selective_state_space_02_gb300 import synth
+    oracle.build()
+    p, cfg = workload_problem(args.workload, 0)
+    import numpy as np
+    nch = p.batch * p.dim
+    arrs = (p.f32("x"), p.f32("delta"), p.A.numpy(), p.f32("B"), p.f32("C"),
+            None if p.D is None else p.D.numpy(), p.f32("z"),
+            None if p.dt_bias is None else p.dt_bias.numpy())
+    threads = oracle.max_threads()
+    # size one step to about 1 s of host work so K + W steps stay within minutes
+    probe = list(range(min(nch, max(threads, 8))))
+    t = time.perf_counter()
+    oracle.fwd(*arrs, p.delta_softplus, channels=probe, return_final_state=False)
+    per_chan = (time.perf_counter() - t) / len(probe)
+    k = int(min(nch, max(len(probe), 1.0 / max(per_chan, 1e-9))))
+    rng = np.random.default_rng(1)
+    steps = []
+    for i in range(args.warmup + args.steps):
+        chans = sorted(rng.choice(nch, k, replace=False).tolist()) if k < nch else None
+        t = time.perf_counter()
+        oracle.fwd(*arrs, p.delta_softplus, channels=chans, return_final_state=False)
+        if i >= args.warmup:
+            steps.append(time.perf_counter() - t)
+    total = sum(steps)
+    value = k * p.seqlen * args.steps / total / 1e9
+    sample = f"{k} of {nch} channels per step (all {p.seqlen} steps each)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": p.batch, "dim": p.dim, "dstate": p.dstate,
+                   "seqlen": p.seqlen, "io_dtype": p.dtype, "gate": p.z is not None},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

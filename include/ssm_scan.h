@@ -146,6 +146,12 @@ int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const
                          int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                          void *workspace, size_t workspace_bytes, void *stream, int variant);
 
+/* Device status of earlier launches on the current device: bit 0 is set when
+ * a kernel's bounded wait on its own TMA copies gave up (the output of that
+ * call is then invalid).  Synchronises `stream`; `clear` nonzero resets the
+ * word.  Returns the status (>= 0) or SSM_ERR_LAUNCH. */
+int ssm_scan_device_status(void *stream, int clear);
+
 /* Device bytes that ssm_scan_fwd_host needs as `device_buffer`: room for the
  * device copies of every input and output plus the variant's workspace,
  * each 256-byte aligned.  Returns (size_t)-1 for invalid sizes. */

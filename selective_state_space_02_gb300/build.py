@@ -48,9 +48,14 @@ def stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
+def _extra_flags():
+    # optional extra nvcc flags, e.g. -DSSM_TUNE for tile-configuration sweeps
+    return os.environ.get("SSM_NVCC_EXTRA", "").split()
+
+
 def _compile(src: str, verbose_ptxas: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *_extra_flags(), "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -174,6 +174,12 @@ int ssm_scan_fwd(const void *x, const void *delta, const float *A, const void *B
                                 stream, SSM_VARIANT_AUTO);
 }
 
+int ssm_scan_device_status(void *stream, int clear) {
+    unsigned int v = 0;
+    if (ssm::read_device_status(static_cast<cudaStream_t>(stream), clear != 0, &v) != 0) return SSM_ERR_LAUNCH;
+    return (int)(v & 0x7fffffffu);
+}
+
 size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                                      int has_D, int has_z, int has_dt_bias, int has_final_state,
                                      int variant) {
