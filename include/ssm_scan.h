@@ -74,7 +74,9 @@ typedef enum {
  *  FUSED   : channel-parallel, time-serial.  Each thread keeps a few states of
  *            one channel in registers and walks the sequence in staged tiles
  *            ("Mamba hardware-aware parallel associative scan", sect. 2.2,
- *            third approach).  No workspace.
+ *            third approach).  Workspace: B and C re-laid out once per call
+ *            as float32 rows (batch * seqlen * (2 * padded dstate + 16) * 4
+ *            bytes, padded dstate = 8, 16, 32 or 64).
  *  CHUNKED : each warp scans a chunk of 32*k steps: every lane runs k steps
  *            serially, a warp-shuffle Hillis-Steele scan combines the lanes'
  *            (a, b) totals, and the state is carried from chunk to chunk
@@ -82,8 +84,8 @@ typedef enum {
  *  TWOPASS : the sequence is cut into chunks processed in parallel; pass 1
  *            writes every chunk's total (A_k, B_k), a small scan over the
  *            chunk totals gives each chunk's start state, and pass 2 re-runs
- *            the fused scan from that state (sect. 2.2, 3.3).  Needs
- *            workspace.
+ *            the fused scan from that state (sect. 2.2, 3.3).  Workspace:
+ *            the chunk totals plus the fused variant's B/C rows.
  *  AUTO    : the library picks one from the shape (ssm_scan_select_variant). */
 typedef enum {
     SSM_VARIANT_AUTO = 0,

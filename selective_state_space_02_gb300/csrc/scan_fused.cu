@@ -52,56 +52,71 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 int padded_states(int N) { return N <= 8 ? 8 : N <= 16 ? 16 : N <= 32 ? 32 : 64; }
 
-// States per lane of cfg 0 (see scan_fused_dispatch.cuh).
-int cfg0_states(int np) { return np == 64 ? 8 : np == 8 ? 2 : 4; }
-
-// cfg 0 when it alone gives about 8 resident consumer warps per SM, else cfg 1.
-int choose_cfg(int64_t nchan, int np, int64_t nseg) {
-#ifdef SSM_TUNE
-    if (const char *e = std::getenv("SSM_FUSED_CFG")) return std::atoi(e);
-#endif
-    const int64_t threads = nchan * nseg * np / cfg0_states(np);
-    return threads >= (int64_t)kSMs * 256 ? 0 : 1;
+// States per lane of each configuration (see scan_fused_dispatch.cuh).
+int fused_states(int np, int cfg, bool tma) {
+    if (np == 8) return (tma && cfg == 0) ? 8 : 4;
+    if (np == 16) return !tma ? 8 : cfg == 0 ? 16 : cfg == 1 ? 8 : 4;
+    if (np == 32) return (tma && cfg == 0) ? 16 : 8;
+    return 16;
 }
 
-// Channels per CTA of the configuration the dispatch will launch
-// (consumer warps x 32 / lanes per channel).
-int tile_channels(int np, int cfg, bool tma) {
-    int s;
-    if (np == 8) s = 2;
-    else if (np == 32) s = 4;
-    else if (np == 16) s = (tma && cfg == 0) ? 4 : 2;
-    else s = (tma && cfg == 0) ? 8 : 4;
-    return 4 * 32 / (np / s);
+int max_cfg(int np) { return np == 16 ? 2 : np == 64 ? 0 : 1; }
+
+// Channels per warp (the TMA box height of x, delta and z).
+int warp_channels(int np, int cfg, bool tma) { return 32 / (np / fused_states(np, cfg, tma)); }
+
+// The configuration with the most states per lane that still gives at least
+// one warp per SM sub-partition (4 per SM); fewer states per lane only when
+// the problem has too few channels for that.
+int choose_cfg(int64_t nchan, int np, int64_t nseg) {
+#ifdef SSM_TUNE
+    if (const char *e = std::getenv("SSM_FUSED_CFG")) {
+        const int c = std::atoi(e);
+        return c < 0 ? 0 : c > max_cfg(np) ? max_cfg(np) : c;
+    }
+#endif
+    for (int cfg = 0; cfg < max_cfg(np); ++cfg) {
+        const int64_t warps = nchan * nseg / warp_channels(np, cfg, true);
+        if (warps >= (int64_t)kSMs * 4) return cfg;
+    }
+    return max_cfg(np);
 }
 
 // Tensor maps for the TMA path; false selects the element-load path (rows not
 // 16-byte aligned, coordinates beyond 32 bits, or no driver entry point).
-bool make_maps(const FwdArgs &a, int cfg, fused::TileMaps &m) {
+bool make_maps(const FwdArgs &a, int cfg, const float *bc, fused::TileMaps &m) {
     std::memset(&m, 0, sizeof(m));
     if (!a.vec16) return false;
     const int64_t rows = (int64_t)a.batch * a.dim;
-    const int64_t brows = (int64_t)a.batch * a.dstate;
+    const int64_t brows = (int64_t)a.batch * a.L;
     if (a.L >= ((int64_t)1 << 31) || rows >= ((int64_t)1 << 31) || brows >= ((int64_t)1 << 31)) return false;
     const int np = padded_states(a.dstate);
-    const uint32_t dt = (uint32_t)tile_channels(np, cfg, true);
+    const uint32_t dt = (uint32_t)(warp_channels(np, cfg, true) * fused::kConsumerWarps);
     const uint64_t L = (uint64_t)a.L;
     const bool bf = a.bf16 != 0;
     const uint32_t tc = (uint32_t)fused::tile_steps(np);
+    const int S = fused_states(np, cfg, true);
+    const int bcw = fused::bc_row(np, S);
     return encode_tile_map(&m.x, a.x, bf, (uint64_t)rows, L, dt, tc) &&
            encode_tile_map(&m.dl, a.delta, bf, (uint64_t)rows, L, dt, tc) &&
-           encode_tile_map(&m.B, a.B, bf, (uint64_t)brows, L, (uint32_t)np, tc) &&
-           encode_tile_map(&m.C, a.C, bf, (uint64_t)brows, L, (uint32_t)np, tc) &&
+           encode_f32_map(&m.bc, bc, (uint64_t)brows, (uint64_t)bcw, tc, (uint32_t)bcw) &&
            (!a.z || encode_tile_map(&m.z, a.z, bf, (uint64_t)rows, L, dt, tc));
 }
 
-cudaError_t launch_mode(const FwdArgs &a, const fused::SegArgs &sg, int mode, int cfg, cudaStream_t st) {
+// Bytes of the prepared B/C rows: [batch * L][widest row] float.
+size_t bc_bytes(int batch, int dstate, int64_t L) {
+    const size_t n = (size_t)batch * (size_t)L * fused::bc_row_max(padded_states(dstate)) * sizeof(float);
+    return (n + 255) / 256 * 256;
+}
+
+cudaError_t launch_mode(const FwdArgs &a, const fused::SegArgs &sg, int mode, int cfg, bool prepare,
+                        cudaStream_t st) {
     unsigned int *status = status_ptr();
     if (!status) return cudaErrorInvalidSymbol;
     fused::TileMaps maps;
-    const bool tma = make_maps(a, cfg, maps);
-    if (a.bf16) return fused::launch_typed<__nv_bfloat16>(a, sg, maps, status, mode, tma, cfg, st);
-    return fused::launch_typed<float>(a, sg, maps, status, mode, tma, cfg, st);
+    const bool tma = make_maps(a, cfg, sg.bc, maps);
+    if (a.bf16) return fused::launch_typed<__nv_bfloat16>(a, sg, maps, status, mode, tma, cfg, prepare, st);
+    return fused::launch_typed<float>(a, sg, maps, status, mode, tma, cfg, prepare, st);
 }
 
 // Small scan over the segment totals ("Mamba hardware-aware parallel
@@ -162,20 +177,40 @@ bool encode_tile_map(CUtensorMap *map, const void *base, bool bf16, uint64_t row
     return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_fused(const FwdArgs &a, cudaStream_t st) {
+bool encode_f32_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t fused_workspace_bytes(int batch, int dim, int dstate, int64_t L) {
+    (void)dim;
+    return bc_bytes(batch, dstate, L);
+}
+
+cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t st) {
     const int64_t nchan = (int64_t)a.batch * a.dim;
-    fused::SegArgs sg{a.L, 1, nullptr, nullptr};
-    return launch_mode(a, sg, fused::kWhole, choose_cfg(nchan, padded_states(a.dstate), 1), st);
+    fused::SegArgs sg{a.L, 1, nullptr, nullptr, static_cast<const float *>(workspace)};
+    return launch_mode(a, sg, fused::kWhole, choose_cfg(nchan, padded_states(a.dstate), 1), true, st);
 }
 
 int64_t twopass_chunk_len(int batch, int dim, int dstate, int64_t L) {
-    // Enough segments that one pass has about 8 CTAs per SM, while each
-    // segment keeps at least 8 tiles of work.
+    // Enough segments that one pass has about 8 warps per SM (counted with
+    // the configuration of fewest channels per warp), while each segment keeps
+    // at least 8 tiles of work.
     const int np = padded_states(dstate);
-    const int dt = tile_channels(np, 1, true);
-    const int64_t ctas = (int64_t)batch * ((dim + dt - 1) / dt);
-    const int64_t want_ctas = (int64_t)kSMs * 8;
-    int64_t nseg = (want_ctas + ctas - 1) / (ctas > 0 ? ctas : 1);
+    const int cpw = warp_channels(np, max_cfg(np), true);
+    const int64_t warps = (int64_t)batch * ((dim + cpw - 1) / cpw);
+    const int64_t want = (int64_t)kSMs * 8;
+    int64_t nseg = (want + warps - 1) / (warps > 0 ? warps : 1);
     const int64_t tcs = fused::tile_steps(np);
     const int64_t max_seg = (L + 8 * tcs - 1) / (8 * tcs);
     if (nseg > max_seg) nseg = max_seg;
@@ -193,7 +228,7 @@ size_t twopass_workspace_bytes(int batch, int dim, int dstate, int64_t L) {
     h = (h + 255) / 256 * 256;
     size_t s = (size_t)nseg * nchan * sizeof(float);
     s = (s + 255) / 256 * 256;
-    return h + s;
+    return h + s + bc_bytes(batch, dstate, L);
 }
 
 cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
@@ -202,15 +237,25 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
     const int64_t nchan = (int64_t)a.batch * a.dim;
     size_t hbytes = (size_t)nseg * nchan * a.dstate * sizeof(float);
     hbytes = (hbytes + 255) / 256 * 256;
-    fused::SegArgs sg{len, nseg, static_cast<float *>(workspace),
-                      reinterpret_cast<float *>(static_cast<char *>(workspace) + hbytes)};
-    const int cfg = choose_cfg(nchan, padded_states(a.dstate), nseg);
+    size_t sbytes = (size_t)nseg * nchan * sizeof(float);
+    sbytes = (sbytes + 255) / 256 * 256;
+    char *ws = static_cast<char *>(workspace);
+    fused::SegArgs sg{len, nseg, reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes),
+                      reinterpret_cast<const float *>(ws + hbytes + sbytes)};
+    // segments already supply the parallelism: the finest lane split measured
+    // fastest for segmented runs
+    int cfg = max_cfg(padded_states(a.dstate));
+#ifdef SSM_TUNE
+    cfg = choose_cfg(nchan, padded_states(a.dstate), nseg);
+#endif
     cudaError_t e = cudaSuccess;
+    bool prepared = false;
     if (nseg > 1) {   // pass 1 over every segment but the last (its total is never used)
         fused::SegArgs s1 = sg;
         s1.nseg = nseg - 1;
-        e = launch_mode(a, s1, fused::kTotals, cfg, st);
+        e = launch_mode(a, s1, fused::kTotals, cfg, true, st);
         if (e != cudaSuccess) return e;
+        prepared = true;
     }
     const int64_t pairs = nchan * a.dstate;
     const int wpb = 8;
@@ -218,7 +263,7 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
                                                                                    a.dim, a.dstate, nseg);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_mode(a, sg, fused::kSeeded, cfg, st);
+    return launch_mode(a, sg, fused::kSeeded, cfg, !prepared, st);
 }
 
 int read_device_status(cudaStream_t st, bool clear, unsigned int *out) {

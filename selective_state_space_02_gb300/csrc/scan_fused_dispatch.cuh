@@ -7,9 +7,14 @@
 namespace ssm {
 namespace fused {
 
-template <typename T, int NP, int S, int NW, bool TMA>
+template <typename T, int NP, int S, bool TMA>
 cudaError_t by_mode(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, unsigned int *status,
-                    int mode, cudaStream_t st) {
+                    int mode, bool prepare, cudaStream_t st) {
+    constexpr int NW = kConsumerWarps;
+    if (prepare) {
+        const cudaError_t e = launch_prepare<T, NP, S>(a, const_cast<float *>(sg.bc), st);
+        if (e != cudaSuccess) return e;
+    }
     const bool gate = a.z != nullptr;
     switch (mode) {
         case kWhole:
@@ -23,30 +28,32 @@ cudaError_t by_mode(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, u
     }
 }
 
-// Tile configurations (states per lane S, consumer warps NW) per padded state
-// count.  cfg 0: more states per lane (fewer threads, cheaper per step);
-// cfg 1: fewer states per lane (twice the threads for narrow problems).  The
-// element-load path (rows not 16-byte aligned) always uses cfg 1.
+// States per lane for a padded state count and configuration index; the
+// configurations trade states per lane (fewer shuffles per update) against
+// lanes per channel (more warps for problems with few channels).  Keep in
+// step with fused_states() in scan_fused.cu.
 template <typename T>
 cudaError_t launch_typed_impl(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps,
-                              unsigned int *status, int mode, bool tma, int cfg, cudaStream_t st) {
+                              unsigned int *status, int mode, bool tma, int cfg, bool prep, cudaStream_t st) {
     const int N = a.dstate;
     if (N <= 8) {
-        return tma ? by_mode<T, 8, 2, 4, true>(a, sg, maps, status, mode, st)
-                   : by_mode<T, 8, 2, 4, false>(a, sg, maps, status, mode, st);
+        if (tma) return cfg == 0 ? by_mode<T, 8, 8, true>(a, sg, maps, status, mode, prep, st)
+                                 : by_mode<T, 8, 4, true>(a, sg, maps, status, mode, prep, st);
+        return by_mode<T, 8, 4, false>(a, sg, maps, status, mode, prep, st);
     }
     if (N <= 16) {
-        if (!tma) return by_mode<T, 16, 2, 4, false>(a, sg, maps, status, mode, st);
-        return cfg == 0 ? by_mode<T, 16, 4, 4, true>(a, sg, maps, status, mode, st)
-                        : by_mode<T, 16, 2, 4, true>(a, sg, maps, status, mode, st);
+        if (tma) return cfg == 0 ? by_mode<T, 16, 16, true>(a, sg, maps, status, mode, prep, st)
+                      : cfg == 1 ? by_mode<T, 16, 8, true>(a, sg, maps, status, mode, prep, st)
+                                 : by_mode<T, 16, 4, true>(a, sg, maps, status, mode, prep, st);
+        return by_mode<T, 16, 8, false>(a, sg, maps, status, mode, prep, st);
     }
     if (N <= 32) {
-        return tma ? by_mode<T, 32, 4, 4, true>(a, sg, maps, status, mode, st)
-                   : by_mode<T, 32, 4, 4, false>(a, sg, maps, status, mode, st);
+        if (tma) return cfg == 0 ? by_mode<T, 32, 16, true>(a, sg, maps, status, mode, prep, st)
+                                 : by_mode<T, 32, 8, true>(a, sg, maps, status, mode, prep, st);
+        return by_mode<T, 32, 8, false>(a, sg, maps, status, mode, prep, st);
     }
-    if (!tma) return by_mode<T, 64, 4, 4, false>(a, sg, maps, status, mode, st);
-    return cfg == 0 ? by_mode<T, 64, 8, 4, true>(a, sg, maps, status, mode, st)
-                    : by_mode<T, 64, 4, 4, true>(a, sg, maps, status, mode, st);
+    return tma ? by_mode<T, 64, 16, true>(a, sg, maps, status, mode, prep, st)
+               : by_mode<T, 64, 16, false>(a, sg, maps, status, mode, prep, st);
 }
 
 }  // namespace fused

@@ -30,13 +30,16 @@ struct FwdArgs {
 };
 
 // Each launcher returns cudaSuccess or the launch error.
-cudaError_t launch_fused(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t s);
 cudaError_t launch_chunked(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t s);
 
 // Device status word of the bounded waits (bit 0: a wait gave up).  Reads it
 // through `st` (synchronising the stream), optionally clearing it.
 int read_device_status(cudaStream_t st, bool clear, unsigned int *out);
+
+// Workspace bytes of the fused variant (B/C prepared as float32 rows).
+size_t fused_workspace_bytes(int batch, int dim, int dstate, int64_t L);
 
 // Chunk length and workspace bytes of the two-pass variant.
 int64_t twopass_chunk_len(int batch, int dim, int dstate, int64_t L);

@@ -81,4 +81,8 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 bool encode_tile_map(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_cols);
 
+// Host: the same for a float32 tensor whose rows hold `cols` values.
+bool encode_f32_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                    uint32_t box_cols);
+
 }  // namespace ssm

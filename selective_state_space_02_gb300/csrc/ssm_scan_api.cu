@@ -72,8 +72,9 @@ int validate(const void *x, const void *delta, const float *A, const void *B, co
 }
 
 size_t workspace_for(int batch, int dim, int dstate, int64_t seqlen, int variant) {
-    if (variant == SSM_VARIANT_TWOPASS && batch > 0 && dim > 0 && seqlen > 0)
-        return ssm::twopass_workspace_bytes(batch, dim, dstate, seqlen);
+    if (batch <= 0 || dim <= 0 || seqlen <= 0) return 0;
+    if (variant == SSM_VARIANT_TWOPASS) return ssm::twopass_workspace_bytes(batch, dim, dstate, seqlen);
+    if (variant == SSM_VARIANT_FUSED) return ssm::fused_workspace_bytes(batch, dim, dstate, seqlen);
     return 0;
 }
 
@@ -104,12 +105,12 @@ const char *ssm_scan_status_string(int status) {
 int ssm_scan_select_variant(int batch, int dim, int dstate, int64_t seqlen, int io_dtype) {
     if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!valid_sizes(batch, dim, dstate, seqlen)) return SSM_ERR_DIMS;
-    // Channel-parallel walking fills the GPU when there are enough channels;
-    // otherwise time must be split: inside a warp (CHUNKED) while there are
-    // still enough channels for one warp each, else across CTAs (TWOPASS).
+    // Channel-parallel walking fills the GPU when there are enough channels
+    // (or the sequence is short); otherwise the sequence is cut into
+    // segments combined by the two-pass chunk carry.  The warp-shuffle
+    // CHUNKED variant is available on request.
     const int64_t nchan = (int64_t)batch * dim;
     if (nchan >= 4096 || seqlen <= 2048) return SSM_VARIANT_FUSED;
-    if (nchan >= 512) return SSM_VARIANT_CHUNKED;
     return SSM_VARIANT_TWOPASS;
 }
 
@@ -157,7 +158,7 @@ int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const
     a.vec16 = v16 ? 1 : 0;
     cudaError_t e;
     switch (v) {
-        case SSM_VARIANT_FUSED: e = ssm::launch_fused(a, st); break;
+        case SSM_VARIANT_FUSED: e = ssm::launch_fused(a, workspace, st); break;
         case SSM_VARIANT_CHUNKED: e = ssm::launch_chunked(a, st); break;
         case SSM_VARIANT_TWOPASS: e = ssm::launch_twopass(a, workspace, st); break;
         default: return SSM_ERR_VARIANT;

@@ -57,17 +57,25 @@ def test_variant_selection_host_only(lib):
     assert ssm.select_variant(4, 1536, 16, 2048) == "fused"
     assert ssm.select_variant(8, 2048, 16, 4096) == "fused"
     assert ssm.select_variant(2, 5120, 64, 8192) == "fused"
-    assert ssm.select_variant(1, 768, 16, 131072) == "chunked"
+    assert ssm.select_variant(1, 768, 16, 131072) == "twopass"
     assert ssm.select_variant(1, 64, 16, 1 << 20) == "twopass"
     assert lib.ssm_scan_select_variant(1, 1, 0, 10, 0) == ERR_DIMS
     assert lib.ssm_scan_select_variant(1, 1, 65, 10, 0) == ERR_DIMS
     assert lib.ssm_scan_select_variant(1, 1, 16, 10, 3) == ERR_DTYPE
 
 
+def _r256(n):
+    return (n + 255) // 256 * 256
+
+
 def test_workspace_sizes(lib):
-    for v in ("fused", "chunked"):
-        assert ssm.workspace_size(4, 1536, 16, 2048, variant=v) == 0
-    assert ssm.workspace_size(1, 64, 16, 0, variant="twopass") == 0
+    assert ssm.workspace_size(4, 1536, 16, 2048, variant="chunked") == 0
+    # fused: B and C prepared once as float32 rows [batch * L][2 * padded dstate + 16]
+    assert ssm.workspace_size(4, 1536, 16, 2048, variant="fused") == _r256(4 * 2048 * 48 * 4)
+    assert ssm.workspace_size(2, 5120, 64, 8192, variant="fused") == _r256(2 * 8192 * 144 * 4)
+    assert ssm.workspace_size(1, 8, 5, 100, variant="fused") == _r256(100 * 32 * 4)
+    for v in ("fused", "twopass"):
+        assert ssm.workspace_size(1, 64, 16, 0, variant=v) == 0
     assert lib.ssm_scan_fwd_workspace_size(1, 1, 99, 10, 0, 0) == (1 << 64) - 1
     assert lib.ssm_scan_fwd_workspace_size(1, 1, 16, 10, 0, 7) == (1 << 64) - 1
 
@@ -86,10 +94,13 @@ def test_twopass_workspace_matches_chunk_state_ledger(lib):
     full = per_chunk * sh["seq_len"]
     assert float(f"{full:.2e}") == pr["elements_all_states"]
     assert round(full * 4 / 1e9, 1) == pr["gb_all_states_fp32"]
-    # our workspace for that shape: K chunk states + K delta sums, 256-byte rounded
+    # our workspace for that shape: K chunk states + K delta sums + the float32
+    # B/C rows of the fused kernel, each 256-byte rounded
     ws = ssm.workspace_size(sh["batch"], sh["d_inner"], sh["d_state"], sh["seq_len"], variant="twopass")
-    r256 = lambda n: (n + 255) // 256 * 256
-    ks = [k for k in range(1, 64) if r256(k * per_chunk * 4) + r256(k * sh["batch"] * sh["d_inner"] * 4) == ws]
+    r256 = _r256
+    bc = r256(sh["batch"] * sh["seq_len"] * (2 * sh["d_state"] + 16) * 4)
+    ks = [k for k in range(1, 64)
+          if r256(k * per_chunk * 4) + r256(k * sh["batch"] * sh["d_inner"] * 4) + bc == ws]
     assert len(ks) == 1, "workspace is not a whole number of chunk states"
     assert ws < full * 4 / 100, "the workspace must stay far below the full state tensor"
 
