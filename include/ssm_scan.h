@@ -67,7 +67,9 @@ typedef enum {
     SSM_ERR_LAUNCH = -6,      /* the CUDA runtime rejected a launch or a copy     */
     SSM_ERR_UNSUPPORTED = -8, /* the variant cannot run this shape                */
     SSM_ERR_ALIAS = -9,       /* an output overlaps an input                      */
-    SSM_ERR_VARIANT = -10     /* unknown variant number                           */
+    SSM_ERR_VARIANT = -10,    /* unknown variant number                           */
+    SSM_ERR_TOO_LARGE = -11   /* problem exceeds the built-in scratch of
+                                 ssm_scan_fwd_noalloc                             */
 } ssm_status_t;
 
 /* Evaluation strategies; all compute the same function.
@@ -176,6 +178,35 @@ int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const vo
                       int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                       void *device_buffer, size_t device_buffer_bytes, void *stream,
                       int variant);
+
+/*
+ * Forward selective scan that allocates nothing (no counterpart in the source
+ * pages; it exists for callers that cannot allocate).
+ *
+ * For callers that cannot call cudaMalloc where they run the scan --
+ * cudaMalloc may synchronise the device and can fail under memory pressure,
+ * which latency-critical serving loops, host callbacks and hosts that hand
+ * over only their input and output buffers cannot afford.  Same arguments,
+ * layouts, validation and result as ssm_scan_fwd_variant(..., FUSED) without
+ * the workspace: the fused kernel's scratch (B and C re-laid out as float32
+ * rows) lives in a 16 MiB device array inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   Limit: batch * seqlen * (2 * padded dstate + 16) * 4 bytes (rounded up to
+ *   256) must not exceed 16 MiB, padded dstate = 8, 16, 32 or 64; larger
+ *   problems return SSM_ERR_TOO_LARGE before anything is launched.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Sharing: all calls on a device use the same array.  Each call rewrites
+ *   the part it reads, so no clearing is needed between calls, but calls that
+ *   overlap on the GPU (different streams, no ordering) race on it and must
+ *   be serialised by the caller.
+ * Allocates no memory, host or device; calls no allocating CUDA routine.
+ */
+int ssm_scan_fwd_noalloc(const void *x, const void *delta, const float *A, const void *B,
+                         const void *C, const float *D, const void *z, const float *dt_bias,
+                         int delta_softplus, void *y, float *final_state,
+                         int batch, int dim, int dstate, int64_t seqlen, int io_dtype, void *stream);
 
 #ifdef __cplusplus
 }

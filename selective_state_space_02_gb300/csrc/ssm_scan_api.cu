@@ -98,6 +98,7 @@ const char *ssm_scan_status_string(int status) {
         case SSM_ERR_UNSUPPORTED: return "the variant cannot run this shape";
         case SSM_ERR_ALIAS: return "an output overlaps an input";
         case SSM_ERR_VARIANT: return "unknown variant";
+        case SSM_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of the allocation-free entry point";
         default: return "unknown status";
     }
 }
