@@ -55,12 +55,17 @@ int padded_states(int N) { return N <= 8 ? 8 : N <= 16 ? 16 : N <= 32 ? 32 : 64;
 // States per lane of each configuration (see scan_fused_dispatch.cuh).
 int fused_states(int np, int cfg, bool tma) {
     if (np == 8) return (tma && cfg == 0) ? 8 : 4;
-    if (np == 16) return !tma ? 8 : cfg == 0 ? 16 : cfg == 1 ? 8 : 4;
+    if (np == 16) return !tma ? 8 : cfg == 0 ? 16 : cfg == 1 ? 8 : cfg == 2 ? 4 : 2;
     if (np == 32) return (tma && cfg == 0) ? 16 : 8;
     return 16;
 }
 
-int max_cfg(int np) { return np == 16 ? 2 : np == 64 ? 0 : 1; }
+int max_cfg(int np) { return np == 16 ? 3 : np == 64 ? 0 : 1; }
+
+// Configuration of the two-pass variant: segments supply the parallelism, and
+// four states per lane (two for N <= 8, eight for N <= 32, sixteen for N <= 64)
+// measured fastest for segmented runs.
+int twopass_cfg(int np) { return np == 16 ? 2 : np == 64 ? 0 : 1; }
 
 // Channels per warp (the TMA box height of x, delta and z).
 int warp_channels(int np, int cfg, bool tma) { return 32 / (np / fused_states(np, cfg, tma)); }
@@ -203,11 +208,10 @@ cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t st) {
 }
 
 int64_t twopass_chunk_len(int batch, int dim, int dstate, int64_t L) {
-    // Enough segments that one pass has about 8 warps per SM (counted with
-    // the configuration of fewest channels per warp), while each segment keeps
-    // at least 8 tiles of work.
+    // Enough segments that one pass has about 8 consumer warps per SM, while
+    // each segment keeps at least 8 tiles of work.
     const int np = padded_states(dstate);
-    const int cpw = warp_channels(np, max_cfg(np), true);
+    const int cpw = warp_channels(np, twopass_cfg(np), true);
     const int64_t warps = (int64_t)batch * ((dim + cpw - 1) / cpw);
     const int64_t want = (int64_t)kSMs * 8;
     int64_t nseg = (want + warps - 1) / (warps > 0 ? warps : 1);
@@ -242,9 +246,7 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
     char *ws = static_cast<char *>(workspace);
     fused::SegArgs sg{len, nseg, reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes),
                       reinterpret_cast<const float *>(ws + hbytes + sbytes)};
-    // segments already supply the parallelism: the finest lane split measured
-    // fastest for segmented runs
-    int cfg = max_cfg(padded_states(a.dstate));
+    int cfg = twopass_cfg(padded_states(a.dstate));
 #ifdef SSM_TUNE
     cfg = choose_cfg(nchan, padded_states(a.dstate), nseg);
 #endif

@@ -44,7 +44,8 @@ cudaError_t launch_typed_impl(const FwdArgs &a, const SegArgs &sg, const TileMap
     if (N <= 16) {
         if (tma) return cfg == 0 ? by_mode<T, 16, 16, true>(a, sg, maps, status, mode, prep, st)
                       : cfg == 1 ? by_mode<T, 16, 8, true>(a, sg, maps, status, mode, prep, st)
-                                 : by_mode<T, 16, 4, true>(a, sg, maps, status, mode, prep, st);
+                      : cfg == 2 ? by_mode<T, 16, 4, true>(a, sg, maps, status, mode, prep, st)
+                                 : by_mode<T, 16, 2, true>(a, sg, maps, status, mode, prep, st);
         return by_mode<T, 16, 8, false>(a, sg, maps, status, mode, prep, st);
     }
     if (N <= 32) {

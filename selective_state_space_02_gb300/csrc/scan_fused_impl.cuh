@@ -12,11 +12,11 @@
 //     ("Mamba (part 2)", scwacadex.pages.dev, sect. 4.1-4.2).
 //
 // Data flow.  A pre-pass (bc_prepare_kernel) writes B and C once per call as
-// float32 rows [batch*L][NS][B(S) C(S) pad(4)] -- per step, per state group,
-// the group's S values of B then of C, zero for padded states, and 16 bytes
-// of padding so that the groups of one step fall in different shared-memory
-// banks -- so that the scan reads each lane's B and C for a step with
-// 16-byte loads, conflict free and without conversion.  The scan CTA has NW consumer warps and one producer warp.
+// float32 rows [batch*L][NS][B(S) C(S) pad] -- per step, per state group,
+// the group's S values of B then of C, zero for padded states, and for groups
+// of 128 bytes 16 bytes of padding so that the groups of one step fall in
+// different shared-memory banks -- so that the scan reads each lane's B and C
+// for a step with 16-byte loads, conflict free and without conversion.  The scan CTA has NW consumer warps and one producer warp.
 //   producer : per tile of TC steps, waits for the ring stage to be free and
 //              issues 2-D TMA copies of x, delta, z (the CTA's DT channel
 //              rows) and of the prepared B/C rows, completing on the stage's
@@ -71,10 +71,13 @@ struct SegArgs {
     const float *bc;   // prepared B/C rows [batch*L][bc_row(NP, S)]
 };
 
-// Floats per prepared B/C row: NS groups of S B values, S C values, 4 pad.
-__host__ __device__ constexpr int bc_group(int S) { return 2 * S + 4; }
+// Floats per prepared B/C row: NS groups of S B values and S C values.  A
+// group of 128 bytes or more (S >= 16) gets 16 bytes of padding so that the
+// groups of one step start in different shared-memory banks; smaller groups
+// already do.
+__host__ __device__ constexpr int bc_group(int S) { return 2 * S + (S >= 16 ? 4 : 0); }
 __host__ __device__ constexpr int bc_row(int NP, int S) { return (NP / S) * bc_group(S); }
-// The widest row over the configurations (at most 4 lanes per channel).
+// The widest row over the configurations.
 __host__ __device__ constexpr int bc_row_max(int NP) { return 2 * NP + 16; }
 
 struct TileMaps {
@@ -253,13 +256,38 @@ __global__ void __launch_bounds__(256) bc_prepare_kernel(const void *Bm, const v
     }
 }
 
+// Reduce-scatter of per-step partial sums over the lanes of a channel.  In
+// the round with xor distance M a lane keeps the half of its current LEN*2
+// steps selected by bit M of its group index and sends the other half, so
+// after log2(NS) rounds v[0..E) holds the full sums of the lane's own steps.
+// Template recursion keeps every index a compile-time constant (registers).
+template <int LEN, int M>
+struct ReduceScatter {
+    template <int NV>
+    static __device__ __forceinline__ void run(float (&v)[NV], int g) {
+        const bool hi = (g & M) != 0;
+#pragma unroll
+        for (int k = 0; k < LEN; ++k) {
+            const float send = hi ? v[k] : v[LEN + k];
+            const float keep = hi ? v[LEN + k] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+        }
+        ReduceScatter<LEN / 2, M / 2>::run(v, g);
+    }
+};
+template <int LEN>
+struct ReduceScatter<LEN, 0> {
+    template <int NV>
+    static __device__ __forceinline__ void run(float (&)[NV], int) {}
+};
+
 template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA>
 __global__ void __launch_bounds__((NW + 1) * 32, SSM_MINB)
 scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps maps, unsigned int *status) {
     using Ly = Layout<T, NP, S, NW, GATE, MODE>;
     constexpr int NS = Ly::NS, CPW = Ly::CPW, DT = Ly::DT, E = Ly::E, TC = Ly::TC;
     constexpr bool kY = Ly::kY, kZ = Ly::kZ;
-    static_assert(S % 2 == 0 && (NS == 1 || NS == 2 || NS == 4), "lane split");
+    static_assert(S % 2 == 0 && (NS == 1 || NS == 2 || NS == 4 || NS == 8), "lane split");
     static_assert(E % 2 == 0 && TC % kBlk == 0, "block split");
     constexpr unsigned FULL = 0xffffffffu;
 
@@ -341,8 +369,11 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
             }
         }
         if constexpr (TMA) {
-            // copies issued before an abort must land before the CTA exits
-            if (lane == 0 && *abort_flag) {
+            // No CTA may exit while its bulk copies are in flight.  The
+            // consumers wait on every tile's barrier; the producer also waits
+            // for the copies it issued last (after an abort they may be the
+            // only waits left) before it returns.
+            if (lane == 0) {
                 for (int t = issued > kNST ? issued - kNST : 0; t < issued; ++t)
                     wait_parity(&full[t % kNST], (uint32_t)((t / kNST) & 1), status, 1ll << 28);
             }
@@ -411,74 +442,68 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
                 }
             }
             // ---- 2. scan the block --------------------------------------------
+            // Batches of JB steps: first everything that does not depend on the
+            // state (Delta/u exchange, B/C loads, a = 2^(Delta A log2 e), u B)
+            // for all JB steps, then the JB dependent updates h = a h + u B and
+            // the contraction.  The independent half gives the scheduler JB
+            // steps of special-function and load latency to overlap.
+            constexpr int JB = S >= 16 ? 2 : 4;
             float pv[kBlk];
 #pragma unroll
-            for (int j = 0; j < kBlk; ++j) {
-                float Dj, Uj;
-                if constexpr (NS == 1) {
-                    Dj = Dl[j];
-                    Uj = Ul[j];
-                } else {
-                    const int src = (lane & ~(NS - 1)) | (j / E);      // owner of step j
-                    Dj = __shfl_sync(FULL, Dl[j % E], src);
-                    Uj = __shfl_sync(FULL, Ul[j % E], src);
-                }
-                const float2 dd = make_float2(Dj, Dj);
-                const float2 uu = make_float2(Uj, Uj);
-                const float *bc = BC + (cb + j) * Ly::BCW + g * bc_group(S);
-                float bcv[2 * S];
+            for (int j0 = 0; j0 < kBlk; j0 += JB) {
+                float2 av[JB][S / 2], bv[JB][S / 2], cv[JB][S / 2];
 #pragma unroll
-                for (int k = 0; k < (kY ? 2 * S : S); k += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4 *>(bc + k);
-                    bcv[k] = v4.x; bcv[k + 1] = v4.y; bcv[k + 2] = v4.z; bcv[k + 3] = v4.w;
-                }
-                // two accumulators halve the dependent chain of the contraction
-                float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
-#pragma unroll
-                for (int q = 0; q < S / 2; ++q) {
-                    const float2 arg = __fmul2_rn(dd, a2[q]);
-                    const float2 a = make_float2(ex2(arg.x), ex2(arg.y));
-                    h2[q] = __ffma2_rn(a, h2[q], __fmul2_rn(uu, make_float2(bcv[2 * q], bcv[2 * q + 1])));
-                    if constexpr (kY) {
-                        const float2 cq = make_float2(bcv[S + 2 * q], bcv[S + 2 * q + 1]);
-                        if (q % 2 == 0) acc0 = __ffma2_rn(cq, h2[q], acc0);
-                        else acc1 = __ffma2_rn(cq, h2[q], acc1);
+                for (int jj = 0; jj < JB; ++jj) {
+                    const int j = j0 + jj;
+                    float Dj, Uj;
+                    if constexpr (NS == 1) {
+                        Dj = Dl[j];
+                        Uj = Ul[j];
+                    } else {
+                        const int src = (lane & ~(NS - 1)) | (j / E);      // owner of step j
+                        Dj = __shfl_sync(FULL, Dl[j % E], src);
+                        Uj = __shfl_sync(FULL, Ul[j % E], src);
                     }
+                    const float2 dd = make_float2(Dj, Dj);
+                    const float2 uu = make_float2(Uj, Uj);
+                    const float *bc = BC + (cb + j) * Ly::BCW + g * bc_group(S);
+                    float bcv[2 * S];
+#pragma unroll
+                    for (int k = 0; k < (kY ? 2 * S : S); k += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4 *>(bc + k);
+                        bcv[k] = v4.x; bcv[k + 1] = v4.y; bcv[k + 2] = v4.z; bcv[k + 3] = v4.w;
+                    }
+#pragma unroll
+                    for (int q = 0; q < S / 2; ++q) {
+                        const float2 arg = __fmul2_rn(dd, a2[q]);
+                        av[jj][q] = make_float2(ex2(arg.x), ex2(arg.y));
+                        bv[jj][q] = __fmul2_rn(uu, make_float2(bcv[2 * q], bcv[2 * q + 1]));
+                        if constexpr (kY) cv[jj][q] = make_float2(bcv[S + 2 * q], bcv[S + 2 * q + 1]);
+                    }
+                    if constexpr (!kY) dsum += Dj;
                 }
-                const float2 acc = __fadd2_rn(acc0, acc1);
-                pv[j] = acc.x + acc.y;
-                if constexpr (!kY) dsum += Dj;
+#pragma unroll
+                for (int jj = 0; jj < JB; ++jj) {
+                    // two accumulators halve the dependent chain of the contraction
+                    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int q = 0; q < S / 2; ++q) {
+                        h2[q] = __ffma2_rn(av[jj][q], h2[q], bv[jj][q]);
+                        if constexpr (kY) {
+                            if (q % 2 == 0) acc0 = __ffma2_rn(cv[jj][q], h2[q], acc0);
+                            else acc1 = __ffma2_rn(cv[jj][q], h2[q], acc1);
+                        }
+                    }
+                    const float2 acc = __fadd2_rn(acc0, acc1);
+                    pv[j0 + jj] = acc.x + acc.y;
+                }
             }
             if constexpr (kY) {
                 // ---- 3. reduce-scatter the partial sums over the NS lanes -------
+                ReduceScatter<kBlk / 2, NS / 2>::run(pv, g);
                 float ys[E];
-                if constexpr (NS == 1) {
 #pragma unroll
-                    for (int k = 0; k < E; ++k) ys[k] = pv[k];
-                } else if constexpr (NS == 2) {
-                    const bool hi = (g & 1) != 0;
-#pragma unroll
-                    for (int k = 0; k < E; ++k) {
-                        const float send = hi ? pv[k] : pv[E + k];
-                        const float keep = hi ? pv[E + k] : pv[k];
-                        ys[k] = keep + __shfl_xor_sync(FULL, send, 1);
-                    }
-                } else {
-                    const bool hi2 = (g & 2) != 0, hi1 = (g & 1) != 0;
-                    float r1[2 * E];
-#pragma unroll
-                    for (int k = 0; k < 2 * E; ++k) {
-                        const float send = hi2 ? pv[k] : pv[2 * E + k];
-                        const float keep = hi2 ? pv[2 * E + k] : pv[k];
-                        r1[k] = keep + __shfl_xor_sync(FULL, send, 2);
-                    }
-#pragma unroll
-                    for (int k = 0; k < E; ++k) {
-                        const float send = hi1 ? r1[k] : r1[E + k];
-                        const float keep = hi1 ? r1[E + k] : r1[k];
-                        ys[k] = keep + __shfl_xor_sync(FULL, send, 1);
-                    }
-                }
+                for (int k = 0; k < E; ++k) ys[k] = pv[k];
                 // ---- skip, gate, store the lane's own steps ---------------------
                 if (dok) {
                     float zv[E];
