@@ -96,7 +96,7 @@ bool make_maps(const FwdArgs &a, int cfg, const float *bc, fused::TileMaps &m) {
     const int64_t brows = (int64_t)a.batch * a.L;
     if (a.L >= ((int64_t)1 << 31) || rows >= ((int64_t)1 << 31) || brows >= ((int64_t)1 << 31)) return false;
     const int np = padded_states(a.dstate);
-    const uint32_t dt = (uint32_t)(warp_channels(np, cfg, true) * fused::kConsumerWarps);
+    const uint32_t dt = (uint32_t)(warp_channels(np, cfg, true) * fused::consumer_warps(fused_states(np, cfg, true)));
     const uint64_t L = (uint64_t)a.L;
     const bool bf = a.bf16 != 0;
     const uint32_t tc = (uint32_t)fused::tile_steps(np);
@@ -208,13 +208,14 @@ cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t st) {
 }
 
 int64_t twopass_chunk_len(int batch, int dim, int dstate, int64_t L) {
-    // Enough segments that one pass has about 8 consumer warps per SM, while
-    // each segment keeps at least 8 tiles of work.
+    // As many segments as keep one pass within about 8 consumer warps per SM
+    // (4 resident CTAs: rounding up would leave a second, nearly empty wave),
+    // while each segment keeps at least 8 tiles of work.
     const int np = padded_states(dstate);
     const int cpw = warp_channels(np, twopass_cfg(np), true);
     const int64_t warps = (int64_t)batch * ((dim + cpw - 1) / cpw);
     const int64_t want = (int64_t)kSMs * 8;
-    int64_t nseg = (want + warps - 1) / (warps > 0 ? warps : 1);
+    int64_t nseg = want / (warps > 0 ? warps : 1);
     const int64_t tcs = fused::tile_steps(np);
     const int64_t max_seg = (L + 8 * tcs - 1) / (8 * tcs);
     if (nseg > max_seg) nseg = max_seg;

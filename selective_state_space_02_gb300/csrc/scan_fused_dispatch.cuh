@@ -10,7 +10,7 @@ namespace fused {
 template <typename T, int NP, int S, bool TMA>
 cudaError_t by_mode(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, unsigned int *status,
                     int mode, bool prepare, cudaStream_t st) {
-    constexpr int NW = kConsumerWarps;
+    constexpr int NW = consumer_warps(S);
     if (prepare) {
         const cudaError_t e = launch_prepare<T, NP, S>(a, const_cast<float *>(sg.bc), st);
         if (e != cudaSuccess) return e;

@@ -24,8 +24,8 @@
 //              loads the tile element by element).
 //   consumers: a consumer warp owns CPW = 32 / NS channels, each channel's NP
 //              (padded) states split over NS lanes, S per lane.  Per block of
-//              kBlk steps:
-//                1. the lane that owns kBlk / NS consecutive steps of its
+//              KB steps (32 when a lane holds at most 4 states, else 16):
+//                1. the lane that owns KB / NS consecutive steps of its
 //                   channel forms Delta = softplus(delta + dt_bias) and
 //                   u = Delta * x for them (packed f32x2, in registers);
 //                2. every lane advances its S recurrences through the block
@@ -49,17 +49,22 @@
 namespace ssm {
 namespace fused {
 
-constexpr int kBlk = 16;           // steps per block (register working set)
 constexpr int kNST = 4;            // TMA ring depth
-constexpr int kConsumerWarps = 2;  // consumer warps per CTA (plus one producer warp)
 
 // Steps per tile (TMA box width): 32, or 16 for wide states so that the
 // ring's B/C tiles stay small.
 __host__ __device__ constexpr int tile_steps(int np) { return np >= 32 ? 16 : 32; }
 
-#ifndef SSM_MINB
-#define SSM_MINB 1
-#endif
+// Steps per block, the register working set of one round of the three
+// phases: fewer block boundaries pay where a lane holds few states, while
+// wider lanes keep 16 to stay within the register budget of 4 CTAs per SM.
+__host__ __device__ constexpr int blk_steps(int S) { return S <= 4 ? 32 : 16; }
+
+// Consumer warps per CTA (plus one producer warp).  Lanes with 16 states need
+// about 160 registers, so 4 CTAs of 2 consumer warps no longer fit on an SM
+// and 3 CTAs of 3 hold more of them at once; narrower lanes fit 4 or 5 CTAs of
+// 2, the finer grain.
+__host__ __device__ constexpr int consumer_warps(int S) { return S >= 16 ? 3 : 2; }
 
 enum Mode { kWhole = 0, kTotals = 1, kSeeded = 2 };
 
@@ -92,7 +97,8 @@ struct Layout {
     static constexpr int CPW = 32 / NS;          // channels per consumer warp
     static constexpr int DT = NW * CPW;          // channels per CTA
     static constexpr int NT = (NW + 1) * 32;     // consumers + producer
-    static constexpr int E = kBlk / NS;          // steps each lane owns per block
+    static constexpr int KB = blk_steps(S);      // steps per block
+    static constexpr int E = KB / NS;            // steps each lane owns per block
     static constexpr int TC = tile_steps(NP);
     static constexpr bool kY = MODE != kTotals;
     static constexpr bool kZ = GATE && kY;
@@ -282,13 +288,14 @@ struct ReduceScatter<LEN, 0> {
 };
 
 template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA>
-__global__ void __launch_bounds__((NW + 1) * 32, SSM_MINB)
+__global__ void __launch_bounds__((NW + 1) * 32, 1)
 scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps maps, unsigned int *status) {
     using Ly = Layout<T, NP, S, NW, GATE, MODE>;
     constexpr int NS = Ly::NS, CPW = Ly::CPW, DT = Ly::DT, E = Ly::E, TC = Ly::TC;
     constexpr bool kY = Ly::kY, kZ = Ly::kZ;
     static_assert(S % 2 == 0 && (NS == 1 || NS == 2 || NS == 4 || NS == 8), "lane split");
-    static_assert(E % 2 == 0 && TC % kBlk == 0, "block split");
+    constexpr int KB = Ly::KB;
+    static_assert(E % 2 == 0 && TC % KB == 0, "block split");
     constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -421,8 +428,8 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
         if (!__all_sync(FULL, ok && *abort_flag == 0)) { aborted = true; break; }
 
 #pragma unroll 1
-        for (int blk = 0; blk < TC / kBlk; ++blk) {
-            const int cb = blk * kBlk;
+        for (int blk = 0; blk < TC / KB; ++blk) {
+            const int cb = blk * KB;
             const int ce = cb + own0;                     // first tile column this lane owns
             // ---- 1. Delta and u of the lane's own E steps (registers) ---------
             float Dl[E], Ul[E], xv[E];
@@ -448,9 +455,9 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
             // the contraction.  The independent half gives the scheduler JB
             // steps of special-function and load latency to overlap.
             constexpr int JB = S >= 16 ? 2 : 4;
-            float pv[kBlk];
+            float pv[KB];
 #pragma unroll
-            for (int j0 = 0; j0 < kBlk; j0 += JB) {
+            for (int j0 = 0; j0 < KB; j0 += JB) {
                 float2 av[JB][S / 2], bv[JB][S / 2], cv[JB][S / 2];
 #pragma unroll
                 for (int jj = 0; jj < JB; ++jj) {
@@ -500,7 +507,7 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
             }
             if constexpr (kY) {
                 // ---- 3. reduce-scatter the partial sums over the NS lanes -------
-                ReduceScatter<kBlk / 2, NS / 2>::run(pv, g);
+                ReduceScatter<KB / 2, NS / 2>::run(pv, g);
                 float ys[E];
 #pragma unroll
                 for (int k = 0; k < E; ++k) ys[k] = pv[k];
