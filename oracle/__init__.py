@@ -76,6 +76,13 @@ def _load():
                                            _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                            ctypes.c_long, _lp, ctypes.c_long, ctypes.c_int]
             lib.ssm_oracle_fwd.restype = ctypes.c_int
+            lib.ssm_oracle_fwd_from.argtypes = [_fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, ctypes.c_int, _dp,
+                                                _dp, _dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+                                                ctypes.c_long, _lp, ctypes.c_long, ctypes.c_int]
+            lib.ssm_oracle_fwd_from.restype = ctypes.c_int
+            lib.ssm_oracle_step.argtypes = [_dp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, ctypes.c_int, _dp,
+                                            ctypes.c_long, ctypes.c_long, ctypes.c_long]
+            lib.ssm_oracle_step.restype = ctypes.c_int
             lib.ssm_oracle_pairs.argtypes = [_fp, _fp, _fp, _fp, _fp, ctypes.c_int,
                                              ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                              ctypes.c_long, ctypes.c_long, ctypes.c_long, _dp, _dp]
@@ -164,13 +171,14 @@ def max_threads() -> int:
 
 
 def fwd(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True,
-        channels=None, nthreads=0, return_final_state=True):
+        channels=None, nthreads=0, return_final_state=True, h0=None):
     """Serial fp64 forward selective scan.
 
     x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L]; A: [dim, dstate];
     D, dt_bias: [dim].  Arrays are read as float32 (bf16 inputs must be passed
     as their exact float32 widening).  ``channels``: optional list of flat
-    channel indices b*dim+d; the result rows follow that order.
+    channel indices b*dim+d; the result rows follow that order.  ``h0``:
+    optional start state [batch, dim, dstate] (read as float64; zeros if None).
     Returns (y [nchan, L] float64, final_state [nchan, dstate] float64 or None).
     """
     x = _f32(x)
@@ -187,6 +195,9 @@ def fwd(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True,
     assert A.shape == (dim, dstate)
     if z is not None:
         assert z.shape == x.shape
+    if h0 is not None:
+        h0 = _f64(h0)
+        assert h0.shape == (batch, dim, dstate)
     if channels is None:
         chan = None
         nchan = batch * dim
@@ -196,14 +207,43 @@ def fwd(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True,
     y = np.empty((nchan, L), np.float64)
     fs = np.empty((nchan, dstate), np.float64) if return_final_state else None
     lp = ctypes.cast(None, _lp) if chan is None else chan.ctypes.data_as(_lp)
-    rc = _load().ssm_oracle_fwd(_ptr(x, _fp), _ptr(delta, _fp), _ptr(A, _fp), _ptr(B, _fp),
-                                _ptr(C, _fp), _ptr(D, _fp), _ptr(z, _fp), _ptr(dt_bias, _fp),
-                                int(bool(delta_softplus)), _ptr(y, _dp),
-                                _ptr(fs, _dp) if fs is not None else ctypes.cast(None, _dp),
-                                batch, dim, dstate, L, lp, nchan, int(nthreads))
+    rc = _load().ssm_oracle_fwd_from(_ptr(x, _fp), _ptr(delta, _fp), _ptr(A, _fp), _ptr(B, _fp),
+                                     _ptr(C, _fp), _ptr(D, _fp), _ptr(z, _fp), _ptr(dt_bias, _fp),
+                                     int(bool(delta_softplus)), _ptr(h0, _dp), _ptr(y, _dp),
+                                     _ptr(fs, _dp) if fs is not None else ctypes.cast(None, _dp),
+                                     batch, dim, dstate, L, lp, nchan, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle forward failed: {rc}")
     return y, fs
+
+
+def step(state, x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True):
+    """One token of the recurrence (decode mode), fp64.
+
+    state: [batch, dim, dstate] (read as float64, not modified); x, delta, z:
+    [batch, dim]; B, C: [batch, dstate]; A: [dim, dstate]; D, dt_bias: [dim].
+    Returns (new_state [batch, dim, dstate] float64, y [batch, dim] float64).
+    """
+    h = np.array(state, dtype=np.float64, copy=True, order="C")
+    x = _f32(x)
+    delta = _f32(delta)
+    A = _f32(A)
+    B = _f32(B)
+    C = _f32(C)
+    D = _f32(D)
+    z = _f32(z)
+    dt_bias = _f32(dt_bias)
+    batch, dim = x.shape
+    dstate = A.shape[1]
+    assert h.shape == (batch, dim, dstate) and delta.shape == x.shape
+    assert B.shape == (batch, dstate) and C.shape == B.shape and A.shape == (dim, dstate)
+    y = np.empty((batch, dim), np.float64)
+    rc = _load().ssm_oracle_step(_ptr(h, _dp), _ptr(x, _fp), _ptr(delta, _fp), _ptr(A, _fp), _ptr(B, _fp),
+                                 _ptr(C, _fp), _ptr(D, _fp), _ptr(z, _fp), _ptr(dt_bias, _fp),
+                                 int(bool(delta_softplus)), _ptr(y, _dp), batch, dim, dstate)
+    if rc != 0:
+        raise RuntimeError(f"oracle step failed: {rc}")
+    return h, y
 
 
 def pairs(x, delta, A, B, dt_bias, delta_softplus, b, d, n):

@@ -15,7 +15,8 @@
  *   [P3] "Mamba (part 2): parallel scan and hardware-aware optimisation"
  *        (scwacadex.pages.dev, blog8_mamba_parallel_scan)
  *        sect. 2.1-2.3 (operator (x), associativity proof),
- *        sect. 2.4 (tree reduction), sect. 4.3 (chunk-boundary states).
+ *        sect. 2.4 (tree reduction), sect. 4.3 (chunk-boundary states),
+ *        sect. 6-7 (inference runs the recurrence one token at a time).
  *
  * Everything is computed in IEEE double with the plain definitions; nothing
  * is blocked, fused or reordered beyond what the cited definition states.
@@ -196,7 +197,9 @@ double ssm_oracle_silu(double z)
 /* ------------------------------------------------------------------ */
 
 /*
- * For every channel (b, d), with h[n] = 0 at the start:
+ * For every channel (b, d), with h[n] = h0[b,d,n] at the start (0 when h0 is
+ * NULL; a given start state is how a sequence resumes from the boundary state
+ * of the segment before it, [P3 sect. 4.3]):
  *   v      = delta[b,d,t] + dt_bias[d]                  (dt_bias optional)
  *   Delta  = softplus(v) if `softplus` else v
  *   a_n    = exp(Delta * A[d,n]),  b_n = Delta * B[b,n,t] * x[b,d,t]
@@ -207,7 +210,7 @@ double ssm_oracle_silu(double z)
  * and final_state[b,d,n] = h[n] after the last step.
  *
  * Layouts (row-major): x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L];
- * A: [dim, dstate]; D, dt_bias: [dim].
+ * A: [dim, dstate]; D, dt_bias: [dim]; h0: [batch, dim, dstate] (double).
  *
  * `chan` selects which channels (index b*dim + d) to evaluate; NULL means all
  * channels in order.  y is written as [nchan, L] and final_state as
@@ -216,12 +219,12 @@ double ssm_oracle_silu(double z)
  * the same serial loop); 0 leaves the OpenMP default.
  * Returns 0, or -1 on bad arguments.
  */
-int ssm_oracle_fwd(const float *x, const float *delta, const float *A,
-                   const float *Bm, const float *Cm, const float *Dskip,
-                   const float *z, const float *dt_bias, int softplus,
-                   double *y, double *final_state,
-                   long batch, long dim, long dstate, long L,
-                   const long *chan, long nchan, int nthreads)
+int ssm_oracle_fwd_from(const float *x, const float *delta, const float *A,
+                        const float *Bm, const float *Cm, const float *Dskip,
+                        const float *z, const float *dt_bias, int softplus,
+                        const double *h0, double *y, double *final_state,
+                        long batch, long dim, long dstate, long L,
+                        const long *chan, long nchan, int nthreads)
 {
     if (!x || !delta || !A || !Bm || !Cm || !y) return -1;
     if (batch <= 0 || dim <= 0 || dstate <= 0 || L < 0) return -1;
@@ -246,6 +249,8 @@ int ssm_oracle_fwd(const float *x, const float *delta, const float *A,
             err = 1;
             continue;
         }
+        if (h0)
+            for (long n = 0; n < dstate; ++n) h[n] = h0[(size_t)c * (size_t)dstate + (size_t)n];
         const float *xr = x + (size_t)c * (size_t)L;
         const float *dr = delta + (size_t)c * (size_t)L;
         const float *zr = z ? z + (size_t)c * (size_t)L : NULL;
@@ -276,6 +281,60 @@ int ssm_oracle_fwd(const float *x, const float *delta, const float *A,
         free(h);
     }
     return err ? -1 : 0;
+}
+
+/* The forward from the zero state. */
+int ssm_oracle_fwd(const float *x, const float *delta, const float *A,
+                   const float *Bm, const float *Cm, const float *Dskip,
+                   const float *z, const float *dt_bias, int softplus,
+                   double *y, double *final_state,
+                   long batch, long dim, long dstate, long L,
+                   const long *chan, long nchan, int nthreads)
+{
+    return ssm_oracle_fwd_from(x, delta, A, Bm, Cm, Dskip, z, dt_bias, softplus, NULL, y,
+                               final_state, batch, dim, dstate, L, chan, nchan, nthreads);
+}
+
+/*
+ * One token of the recurrence for every channel: the recurrent (decode) mode
+ * in which inference advances the state one step at a time with constant
+ * work and memory per token ([P3 sect. 6-7]).  With s = state[b,d,:]:
+ *   Delta     = softplus(delta[b,d] + dt_bias[d])   (or without softplus)
+ *   s[k]     <- exp(Delta * A[d,k]) * s[k] + Delta * B[b,k] * x[b,d]
+ *   y[b,d]    = (sum_k C[b,k] * s[k] + D[d] * x[b,d]) * silu(z[b,d])
+ * D, z and dt_bias are optional.  The arithmetic is that of one iteration of
+ * the forward above, in the same order, so L calls reproduce a forward over L
+ * steps exactly.
+ * Layouts: state [batch, dim, dstate] (double, updated in place);
+ * x, delta, z [batch, dim]; B, C [batch, dstate]; A [dim, dstate];
+ * D, dt_bias [dim]; y [batch, dim].  Returns 0, or -1 on bad arguments.
+ */
+int ssm_oracle_step(double *state, const float *x, const float *delta, const float *A,
+                    const float *Bv, const float *Cv, const float *Dskip, const float *z,
+                    const float *dt_bias, int softplus, double *y,
+                    long batch, long dim, long dstate)
+{
+    if (!state || !x || !delta || !A || !Bv || !Cv || !y) return -1;
+    if (batch < 0 || dim < 0 || dstate <= 0) return -1;
+    for (long c = 0; c < batch * dim; ++c) {
+        long bb = c / dim, d = c % dim;
+        double xin = (double)x[c];
+        double arg = (double)delta[c] + (dt_bias ? (double)dt_bias[d] : 0.0);
+        double step = softplus ? ssm_oracle_softplus(arg) : arg;
+        double skip = Dskip ? (double)Dskip[d] : 0.0;
+        double *s = state + (size_t)c * (size_t)dstate;
+        double out = 0.0;
+        for (long k = 0; k < dstate; ++k) {
+            double decay = exp(step * (double)A[(size_t)d * (size_t)dstate + (size_t)k]);
+            double inject = step * (double)Bv[(size_t)bb * (size_t)dstate + (size_t)k] * xin;
+            s[k] = decay * s[k] + inject;
+            out += (double)Cv[(size_t)bb * (size_t)dstate + (size_t)k] * s[k];
+        }
+        out = out + skip * xin;
+        if (z) out *= ssm_oracle_silu((double)z[c]);
+        y[c] = out;
+    }
+    return 0;
 }
 
 /* The per-step pairs (a_t, b_t) of one recurrence (b, d, n), t = 0..L-1, as

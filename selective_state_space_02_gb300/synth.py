@@ -159,3 +159,20 @@ def min_bytes(p: Problem) -> int:
     if p.final_state:
         n += p.batch * p.dim * p.dstate * 4
     return n
+
+
+def make_state(batch: int, dim: int, dstate: int, seed: int = 0, scale: float = 1.0) -> torch.Tensor:
+    """A start state [batch, dim, dstate] float32 drawn N(0, scale^2): the
+    boundary state a resumed segment or a decode session begins from."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = rng.standard_normal((batch, dim, dstate), dtype=np.float32) * np.float32(scale)
+    return torch.from_numpy(np.ascontiguousarray(s))
+
+
+def step_inputs(p: Problem, t: int) -> dict:
+    """The inputs of token t of problem p for a single decode step: x, delta
+    and z as [batch, dim], B and C as [batch, dstate] (contiguous copies in the
+    I/O dtype), plus the per-channel parameters."""
+    col = lambda a: None if a is None else a[:, :, t].contiguous()
+    return dict(x=col(p.x), delta=col(p.delta), z=col(p.z), B=col(p.B), C=col(p.C),
+                A=p.A, D=p.D, dt_bias=p.dt_bias)
