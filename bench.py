@@ -7,6 +7,11 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--variant auto|fused|chunked|twopass] [--impl ours|reference]
+                  [--op fwd|step]
+
+``--op step`` times the single-token decode step (ssm_scan_step) on the
+decode workload instead: one step = one token for every sequence of the
+batch, the state resident in HBM, reported against the HBM roofline.
 
 N > 1 runs under torch.distributed.run, one rank per GPU: every rank scans its
 own batch of the same shape (weak scaling, no data-path collective); the
@@ -65,6 +70,7 @@ def parse_args(argv=None):
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clock sampling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default="fwd", choices=["fwd", "step"])
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -209,6 +215,19 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+L2_NOTE = ("flushed between timed steps: a {mib} MiB write, then a read of the same buffer so that no "
+           "dirty line of it is left to be written back during the timed kernel; outside the timed events")
+
+
+def flush_l2(buf):
+    """Evict the workload from L2: write a buffer larger than L2, then read
+    it back so that L2 ends up holding clean lines of that buffer (the write
+    alone would leave ~129 MB of dirty lines whose write-back lands inside
+    the next timed step)."""
+    buf.zero_()
+    buf.view(-1).max()
+
+
 def workload_problem(name: str, rank: int):
     from selective_state_space_02_gb300 import synth
     cfg = dict(synth.WORKLOADS[name])
@@ -272,7 +291,7 @@ def run_ours(args):
                      return_final_state=fs is not None, variant=variant, y=y, final_state=fs, workspace=ws)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2(flush)
         step()
     torch.cuda.synchronize()
 
@@ -281,7 +300,7 @@ def run_ours(args):
     t_end = time.time() + args.soak_s
     while time.time() < t_end:          # untimed load: clocks settle, sampler sees the load
         for _ in range(20):
-            flush.zero_()
+            flush_l2(flush)
             step()
         torch.cuda.synchronize()
 
@@ -290,7 +309,7 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.zero_()                   # L2 flush, outside the timed events
+        flush_l2(flush)                 # L2 flush, outside the timed events
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -365,7 +384,7 @@ def run_ours(args):
         "config": {"workload": args.workload, "batch": p.batch, "dim": p.dim, "dstate": p.dstate,
                    "seqlen": p.seqlen, "io_dtype": p.dtype, "gate": p.z is not None,
                    "final_state": p.final_state, "variant": variant,
-                   "l2": f"flushed between timed steps ({args.flush_mib} MiB write, outside the timed events)",
+                   "l2": L2_NOTE.format(mib=args.flush_mib),
                    "parallelism": f"{world} independent replicas, one batch each" if world > 1 else "single GPU"},
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -426,10 +445,144 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------ decode step
+STEP_METRIC = "decode step: channel-tokens/s (B·D per step) and achieved HBM GB/s as % of GB300 roofline"
+STEP_UNIT = "Gtoken-channels/s"
+
+
+def step_problem(name: str, rank: int):
+    from selective_state_space_02_gb300 import synth
+    cfg = dict(synth.STEP_WORKLOADS[name])
+    cfg["seed"] = rank_seed(cfg["seed"], rank)
+    p = synth.make_problem(**cfg)
+    return p, synth.make_state(p.batch, p.dim, p.dstate, seed=cfg["seed"] + 1)
+
+
+def step_cpu_baseline(p, h0, reps: int = 3):
+    """The fp64 oracle step over the whole decode batch, a few times."""
+    import oracle
+    from selective_state_space_02_gb300 import synth
+    oracle.build()
+    s = synth.step_inputs(p, 0)
+    f = lambda v: None if v is None else v.float().numpy()
+    h = h0.numpy().astype("float64")
+    t = time.perf_counter()
+    for _ in range(reps):
+        h, _ = oracle.step(h, f(s["x"]), f(s["delta"]), p.A.numpy(), f(s["B"]), f(s["C"]),
+                           None if p.D is None else p.D.numpy(), f(s["z"]),
+                           None if p.dt_bias is None else p.dt_bias.numpy(), p.delta_softplus)
+    dt = (time.perf_counter() - t) / reps
+    return {"value": p.batch * p.dim / dt / 1e9, "unit": STEP_UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"whole decode batch ({p.batch} x {p.dim} channels), {reps} steps, serial"}
+
+
+def run_step(args):
+    import torch
+    import selective_state_space_02_gb300 as ssm
+    from selective_state_space_02_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    name = args.workload if args.workload in synth.STEP_WORKLOADS else "decode_bf16"
+    p, h0 = step_problem(name, rank)
+    s = {k: (v.to(dev) if v is not None else None) for k, v in synth.step_inputs(p, 0).items()}
+    state = h0.to(dev)
+    y = torch.empty_like(s["x"])
+    flush = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssm.scan_step(state, s["x"], s["delta"], s["A"], s["B"], s["C"], D=s["D"], z=s["z"], dt_bias=s["dt_bias"],
+                      delta_softplus=p.delta_softplus, y=y)
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.time() + args.soak_s
+    while time.time() < t_end:
+        for _ in range(20):
+            flush_l2(flush)
+            step()
+        torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush_l2(flush)                 # L2 flush (the 34 MB state would otherwise stay in L2)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    per = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(per), world, dev)
+    chans = p.batch * p.dim
+    value = world * chans * args.steps / (total_ms / 1e3) / 1e9
+    hbm_peak, peak_kind = measured_peaks()
+    mb = synth.step_min_bytes(p)
+    kern_s = statistics.mean(per) / 1e3
+    roofline = {"bound": "hbm", "achieved": round(mb / kern_s / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(mb / kern_s / 1e9 / hbm_peak, 4), "traffic": None,
+                "kernel": "decode step (ssm_scan_step)", "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": mb}
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: None if t is None else t.pin_memory()
+        hs = {k: pin(v) for k, v in synth.step_inputs(p, 0).items()
+              if k in ("x", "delta", "z", "B", "C") and v is not None}
+        hy = torch.empty_like(hs["x"]).pin_memory()
+
+        def hstep():
+            for k, v in hs.items():
+                s[k].copy_(v, non_blocking=True)
+            step()
+            hy.copy_(y, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(args.warmup):
+            hstep()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            hstep()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": world * chans * args.steps / t_e2e / 1e9, "unit": STEP_UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in hs.values()),
+               "d2h_bytes_per_step": hy.numel() * hy.element_size(),
+               "api": "scan_step with the token's inputs copied from pinned host memory and y copied back"}
+    cpu = step_cpu_baseline(p, h0) if rank == 0 and world == 1 and not args.no_cpu_baseline else None
+    line = {
+        "metric": STEP_METRIC, "value": round(value, 3), "unit": STEP_UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "batch": p.batch, "dim": p.dim, "dstate": p.dstate, "io_dtype": p.dtype,
+                   "gate": p.z is not None,
+                   "l2": L2_NOTE.format(mib=args.flush_mib),
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "step":
+        run_step(args)
     else:
         run_ours(args)
 

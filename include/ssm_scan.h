@@ -150,6 +150,27 @@ int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const
                          int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                          void *workspace, size_t workspace_bytes, void *stream, int variant);
 
+/*
+ * Forward selective scan from a given start state: h_{-1} = initial_state
+ * instead of 0, everything else as ssm_scan_fwd_variant.  A long sequence cut
+ * into segments is scanned one segment per call, each call starting from the
+ * state the previous one ended in -- the boundary state a segment restarts
+ * from in "Mamba (part 2)" sect. 4.3 -- so that the concatenated y equals one
+ * call over the whole sequence up to float32 rounding.
+ *   initial_state  optional input (NULL: zero state, identical to
+ *                  ssm_scan_fwd_variant).  [batch, dim, dstate] float32,
+ *                  4-byte aligned.  It must not overlap y.  final_state may be
+ *                  the same array (the state is then advanced in place) but
+ *                  must not overlap it otherwise (SSM_ERR_ALIAS).
+ *   seqlen == 0    final_state, if given, receives initial_state (or 0).
+ * The workspace size is that of ssm_scan_fwd_workspace_size for the variant.
+ */
+int ssm_scan_fwd_from_state(const void *x, const void *delta, const float *A, const void *B,
+                            const void *C, const float *D, const void *z, const float *dt_bias,
+                            int delta_softplus, const float *initial_state, void *y, float *final_state,
+                            int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                            void *workspace, size_t workspace_bytes, void *stream, int variant);
+
 /* Device status of earlier launches on the current device: bit 0 is set when
  * a kernel's bounded wait on its own TMA copies gave up (the output of that
  * call is then invalid).  Synchronises `stream`; `clear` nonzero resets the

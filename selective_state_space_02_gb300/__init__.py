@@ -14,7 +14,7 @@ import torch
 from . import _native
 from ._native import ScanError, VARIANTS, SSM_BF16, SSM_F32
 
-__all__ = ["scan_fwd", "scan_fwd_host", "select_variant", "workspace_size", "ScanError",
+__all__ = ["scan_fwd", "scan_fwd_host", "scan_step", "select_variant", "workspace_size", "ScanError",
            "VARIANTS", "host_buffer_size"]
 
 
@@ -98,16 +98,27 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
              C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
              dt_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
              return_final_state: bool = False, variant="auto", y: Optional[torch.Tensor] = None,
-             final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+             final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+             initial_state: Optional[torch.Tensor] = None):
     """Forward selective scan on CUDA tensors, launched on the current stream.
 
     x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (float32 or
     bfloat16, all the same); A: [dim, dstate], D, dt_bias: [dim] (float32).
     Returns y (same dtype as x), or (y, final_state [batch, dim, dstate]
     float32) when ``return_final_state``.  ``y``, ``final_state`` and
-    ``workspace`` may be given to avoid allocations.
+    ``workspace`` may be given to avoid allocations.  ``initial_state``
+    [batch, dim, dstate] float32 starts the recurrence from that state (a
+    resumed segment); ``final_state`` may be the same tensor to advance it in
+    place.
     """
     batch, dim, N, L = _check_inputs(x, delta, A, B, C, D, z, dt_bias, "cuda")
+    if initial_state is not None:
+        if initial_state.dtype != torch.float32:
+            raise TypeError("initial_state must be float32")
+        if not initial_state.is_contiguous() or initial_state.device.type != "cuda":
+            raise ValueError("initial_state must be a contiguous CUDA tensor")
+        if initial_state.shape != (batch, dim, N):
+            raise ValueError("initial_state must be [batch, dim, dstate]")
     lib = _native.load()
     code = _dtype_code(x.dtype)
     v = _variant_code(variant)
@@ -121,12 +132,16 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
     stream = torch.cuda.current_stream(x.device).cuda_stream
-    rc = lib.ssm_scan_fwd_variant(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                                  _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y),
-                                  _ptr(final_state) if return_final_state else None,
-                                  batch, dim, N, L, code,
-                                  _ptr(workspace) if ws_bytes else None,
-                                  ws_bytes, stream, v)
+    fs = _ptr(final_state) if return_final_state else None
+    ws = _ptr(workspace) if ws_bytes else None
+    if initial_state is None:
+        rc = lib.ssm_scan_fwd_variant(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                      _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), fs,
+                                      batch, dim, N, L, code, ws, ws_bytes, stream, v)
+    else:
+        rc = lib.ssm_scan_fwd_from_state(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                         _ptr(dt_bias), int(bool(delta_softplus)), _ptr(initial_state),
+                                         _ptr(y), fs, batch, dim, N, L, code, ws, ws_bytes, stream, v)
     _native.check(rc)
     if return_final_state:
         return y, final_state
@@ -157,5 +172,42 @@ def scan_fwd_host(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torc
     rc = lib.ssm_scan_fwd_host(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), _ptr(final_state),
                                batch, dim, N, L, code, _ptr(device_buffer), need, stream.cuda_stream, v)
+    _native.check(rc)
+    return y
+
+
+def scan_step(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor,
+              B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
+              z: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+              delta_softplus: bool = True, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step on CUDA tensors (include/ssm_step.h): advances
+    ``state`` [batch, dim, dstate] float32 in place by one token and returns
+    y [batch, dim].  x, delta, z: [batch, dim]; B, C: [batch, dstate] (float32
+    or bfloat16, all the same); A: [dim, dstate], D, dt_bias: [dim] float32."""
+    io = x.dtype
+    code = _dtype_code(io)
+    for name, t in (("delta", delta), ("B", B), ("C", C), ("z", z)):
+        if t is not None and t.dtype != io:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected {io}")
+    for name, t in (("state", state), ("A", A), ("D", D), ("dt_bias", dt_bias)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    for name, t in (("state", state), ("x", x), ("delta", delta), ("A", A), ("B", B), ("C", C),
+                    ("D", D), ("z", z), ("dt_bias", dt_bias)):
+        if t is not None and (not t.is_contiguous() or t.device.type != "cuda"):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if x.dim() != 2:
+        raise ValueError("x must be [batch, dim]")
+    batch, dim = x.shape
+    N = A.shape[1]
+    if state.shape != (batch, dim, N) or delta.shape != x.shape or (z is not None and z.shape != x.shape):
+        raise ValueError("state must be [batch, dim, dstate]; delta and z [batch, dim]")
+    if A.shape != (dim, N) or B.shape != (batch, N) or C.shape != (batch, N):
+        raise ValueError("A must be [dim, dstate]; B and C [batch, dstate]")
+    if y is None:
+        y = torch.empty_like(x)
+    rc = _native.load().ssm_scan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                      _ptr(z), _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), batch, dim,
+                                      N, code, torch.cuda.current_stream(x.device).cuda_stream)
     _native.check(rc)
     return y

@@ -37,6 +37,10 @@ SIGNATURES = {
     "ssm_scan_fwd_host_buffer_size": (_sz, [_i, _i, _i, _i64, _i, _i, _i, _i, _i, _i]),
     "ssm_scan_fwd_host": (_i, list(_FWD_ARGS) + [_i]),
     "ssm_scan_fwd_noalloc": (_i, list(_FWD_ARGS[:16]) + [_vp]),
+    # x..softplus, initial_state, y, final_state, sizes, dtype, workspace, bytes, stream, variant
+    "ssm_scan_fwd_from_state": (_i, list(_FWD_ARGS[:9]) + [_vp] + list(_FWD_ARGS[9:]) + [_i]),
+    # state, x, delta, A, B, C, D, z, dt_bias, softplus, y, batch, dim, dstate, dtype, stream
+    "ssm_scan_step": (_i, [_vp] * 9 + [_i, _vp, _i, _i, _i, _i, _vp]),
 }
 
 

@@ -99,7 +99,7 @@ chunked_scan_kernel(FwdArgs p) {
     const int64_t L = p.L;
     const bool vec16 = p.vec16 != 0;
     float *carry = carry_sm[w];
-    for (int n = lane; n < N; n += 32) carry[n] = 0.0f;
+    for (int n = lane; n < N; n += 32) carry[n] = p.h0 ? p.h0[ch * N + n] : 0.0f;
     __syncwarp();
 
     const float bias = p.dt_bias ? __ldg(p.dt_bias + d) : 0.0f;

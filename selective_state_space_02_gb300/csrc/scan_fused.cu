@@ -129,16 +129,17 @@ cudaError_t launch_mode(const FwdArgs &a, const fused::SegArgs &sg, int mode, in
 // state): the segment pairs (A_k, B_k) = (exp(A * sum Delta_k), h_end_k) are
 // combined with a warp-shuffle Hillis-Steele scan, 32 segments per round, the
 // running state carried from round to round.  On return ws_h[k] holds the
-// state at the start of segment k, h_init^(k), with h_init^(0) = 0.
+// state at the start of segment k, h_init^(k), with h_init^(0) the start state
+// h0 of the whole sequence (zero when h0 is null).
 __global__ void segment_carry_kernel(const float *__restrict__ A, float *ws_h, const float *__restrict__ ws_s,
-                                     int64_t nchan, int dim, int N, int nseg) {
+                                     const float *__restrict__ h0, int64_t nchan, int dim, int N, int nseg) {
     const int lane = threadIdx.x & 31;
     const int64_t pair = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (pair >= nchan * N) return;                 // whole warp leaves together
     const int64_t ch = pair / N;
     const int n = (int)(pair % N);
     const float a2 = A[(int64_t)(ch % dim) * N + n] * kLog2e;
-    float carry = 0.0f;                             // h_init of the first segment of the round
+    float carry = h0 ? h0[ch * N + n] : 0.0f;       // h_init of the first segment of the round
     for (int k0 = 0; k0 < nseg; k0 += 32) {
         const int k = k0 + lane;
         float Ak = 1.0f, Bk = 0.0f;                 // identity pads the round
@@ -262,12 +263,14 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
     }
     const int64_t pairs = nchan * a.dstate;
     const int wpb = 8;
-    segment_carry_kernel<<<(unsigned)((pairs + wpb - 1) / wpb), wpb * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, nchan,
-                                                                                   a.dim, a.dstate, nseg);
+    segment_carry_kernel<<<(unsigned)((pairs + wpb - 1) / wpb), wpb * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, a.h0,
+                                                                                   nchan, a.dim, a.dstate, nseg);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_mode(a, sg, fused::kSeeded, cfg, !prepared, st);
 }
+
+unsigned int *device_status_word() { return status_ptr(); }
 
 int read_device_status(cudaStream_t st, bool clear, unsigned int *out) {
     unsigned int *p = status_ptr();

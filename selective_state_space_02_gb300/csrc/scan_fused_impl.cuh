@@ -406,7 +406,9 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
             const int n = g * S + 2 * q + k;
             const bool ok = dok && n < N;
             v[k] = ok ? __ldg(p.A + (int64_t)d * N + n) * kLog2e : 0.0f;
-            hv[k] = (MODE == kSeeded && ok) ? sg.ws_h[((int64_t)seg * nchan + chan0 + d) * N + n] : 0.0f;
+            hv[k] = (MODE == kSeeded && ok)               ? sg.ws_h[((int64_t)seg * nchan + chan0 + d) * N + n]
+                    : (MODE == kWhole && ok && p.h0)     ? p.h0[(chan0 + d) * N + n]
+                                                         : 0.0f;
         }
         a2[q] = make_float2(v[0], v[1]);
         h2[q] = make_float2(hv[0], hv[1]);

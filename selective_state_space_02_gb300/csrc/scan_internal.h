@@ -27,12 +27,17 @@ struct FwdArgs {
     int64_t L;
     int bf16;              // 1: io elements are bf16, 0: float32
     int vec16;             // 1: every io row starts 16-byte aligned
+    const float *h0 = nullptr;   // nullable start state [batch, dim, dstate]; zeros if null
 };
 
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t s);
 cudaError_t launch_chunked(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t s);
+
+// Device address of the status word of the bounded waits on the current
+// device (nullptr if the lookup fails); kernels OR bit 0 into it.
+unsigned int *device_status_word();
 
 // Device status word of the bounded waits (bit 0: a wait gave up).  Reads it
 // through `st` (synchronising the stream), optionally clearing it.

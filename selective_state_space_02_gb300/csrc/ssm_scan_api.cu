@@ -34,10 +34,12 @@ Range range_of(const void *p, size_t bytes) {
 
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
-// Shared validation of both entry points.  Returns SSM_OK or an error code.
+// Shared validation of the entry points.  Returns SSM_OK or an error code.
+// The start state h0 (nullable) is an input that final_state may replace in
+// place: the two may be the same array, but no other overlap is allowed.
 int validate(const void *x, const void *delta, const float *A, const void *B, const void *C,
              const float *D, const void *z, const float *dt_bias, void *y, float *final_state,
-             int batch, int dim, int dstate, int64_t seqlen, int io_dtype) {
+             int batch, int dim, int dstate, int64_t seqlen, int io_dtype, const float *h0 = nullptr) {
     if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!valid_sizes(batch, dim, dstate, seqlen)) return SSM_ERR_DIMS;
     // sizes whose element counts would not fit the 64-bit index arithmetic
@@ -51,9 +53,12 @@ int validate(const void *x, const void *delta, const float *A, const void *B, co
     const void *iop[] = {x, delta, B, C, z, y};
     for (const void *q : iop)
         if (q && !aligned(q, es)) return SSM_ERR_ALIGN;
-    const void *fp[] = {A, D, dt_bias, final_state};
+    const void *fp[] = {A, D, dt_bias, final_state, h0};
     for (const void *q : fp)
         if (q && !aligned(q, 4)) return SSM_ERR_ALIGN;
+    const size_t ns = (size_t)batch * dim * dstate * 4;
+    if (h0 && final_state && h0 != final_state && overlap(range_of(h0, ns), range_of(final_state, ns)))
+        return SSM_ERR_ALIAS;
     if (empty || seqlen == 0) return SSM_OK;
     // outputs must not overlap inputs
     const size_t nx = (size_t)batch * dim * (size_t)seqlen * es;
@@ -62,6 +67,7 @@ int validate(const void *x, const void *delta, const float *A, const void *B, co
                          range_of(B, nb), range_of(C, nb),
                          range_of(A, (size_t)dim * dstate * 4), range_of(D, D ? (size_t)dim * 4 : 0),
                          range_of(dt_bias, dt_bias ? (size_t)dim * 4 : 0)};
+    if (h0 && overlap(range_of(y, nx), range_of(h0, ns))) return SSM_ERR_ALIAS;
     const Range outs[] = {range_of(y, nx),
                           range_of(final_state, final_state ? (size_t)batch * dim * dstate * 4 : 0)};
     for (const Range &o : outs)
@@ -124,13 +130,18 @@ size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqle
     return workspace_for(batch, dim, dstate, seqlen, v);
 }
 
-int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const void *B,
-                         const void *C, const float *D, const void *z, const float *dt_bias,
-                         int delta_softplus, void *y, float *final_state,
-                         int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
-                         void *workspace, size_t workspace_bytes, void *stream, int variant) {
+}  // extern "C"
+
+namespace {
+
+// The device-buffer forward behind ssm_scan_fwd_variant and
+// ssm_scan_fwd_from_state; h0 is the nullable start state.
+int fwd_device(const void *x, const void *delta, const float *A, const void *B, const void *C, const float *D,
+               const void *z, const float *dt_bias, int delta_softplus, const float *h0, void *y,
+               float *final_state, int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+               void *workspace, size_t workspace_bytes, void *stream, int variant) {
     int rc = validate(x, delta, A, B, C, D, z, dt_bias, y, final_state, batch, dim, dstate, seqlen,
-                      io_dtype);
+                      io_dtype, h0);
     if (rc != SSM_OK) return rc;
     const int v = resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant);
     if (v < 0) return v;
@@ -139,16 +150,19 @@ int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const
         return SSM_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (batch == 0 || dim == 0) return SSM_OK;
-    if (seqlen == 0) {
-        if (final_state &&
-            cudaMemsetAsync(final_state, 0, (size_t)batch * dim * dstate * sizeof(float), st) != cudaSuccess)
-            return SSM_ERR_LAUNCH;
-        return SSM_OK;
+    if (seqlen == 0) {   // the state is unchanged: final = start (or zero)
+        const size_t ns = (size_t)batch * dim * dstate * sizeof(float);
+        cudaError_t e = cudaSuccess;
+        if (final_state && h0 && final_state != h0)
+            e = cudaMemcpyAsync(final_state, h0, ns, cudaMemcpyDeviceToDevice, st);
+        else if (final_state && !h0)
+            e = cudaMemsetAsync(final_state, 0, ns, st);
+        return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
     }
     ssm::FwdArgs a;
     a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
     a.softplus = delta_softplus ? 1 : 0;
-    a.y = y; a.final_state = final_state;
+    a.y = y; a.final_state = final_state; a.h0 = h0;
     a.batch = batch; a.dim = dim; a.dstate = dstate; a.L = seqlen;
     a.bf16 = io_dtype == SSM_BF16;
     const size_t es = elem_size(io_dtype);
@@ -165,6 +179,28 @@ int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const
         default: return SSM_ERR_VARIANT;
     }
     return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_scan_fwd_variant(const void *x, const void *delta, const float *A, const void *B,
+                         const void *C, const float *D, const void *z, const float *dt_bias,
+                         int delta_softplus, void *y, float *final_state,
+                         int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                         void *workspace, size_t workspace_bytes, void *stream, int variant) {
+    return fwd_device(x, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, y, final_state, batch, dim,
+                      dstate, seqlen, io_dtype, workspace, workspace_bytes, stream, variant);
+}
+
+int ssm_scan_fwd_from_state(const void *x, const void *delta, const float *A, const void *B,
+                            const void *C, const float *D, const void *z, const float *dt_bias,
+                            int delta_softplus, const float *initial_state, void *y, float *final_state,
+                            int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                            void *workspace, size_t workspace_bytes, void *stream, int variant) {
+    return fwd_device(x, delta, A, B, C, D, z, dt_bias, delta_softplus, initial_state, y, final_state, batch,
+                      dim, dstate, seqlen, io_dtype, workspace, workspace_bytes, stream, variant);
 }
 
 int ssm_scan_fwd(const void *x, const void *delta, const float *A, const void *B, const void *C,

@@ -45,6 +45,14 @@ WORKLOADS = {
                             final_state=False, a_scale=0.25, delta="logu", seed=20261206),
 }
 
+# Named decode-step workloads: one token for every sequence of a serving
+# batch, the state [batch, dim, dstate] resident on the device.
+STEP_WORKLOADS = {
+    # 256 sequences x 2048 channels x 16 states, bf16 I/O, gate on
+    "decode_bf16": dict(batch=256, dim=2048, dstate=16, seqlen=1, dtype="bf16", gate=True,
+                        final_state=True, a_scale=1.0, delta="logu", seed=20261210),
+}
+
 
 @dataclasses.dataclass
 class Problem:
@@ -176,3 +184,16 @@ def step_inputs(p: Problem, t: int) -> dict:
     col = lambda a: None if a is None else a[:, :, t].contiguous()
     return dict(x=col(p.x), delta=col(p.delta), z=col(p.z), B=col(p.B), C=col(p.C),
                 A=p.A, D=p.D, dt_bias=p.dt_bias)
+
+
+def step_min_bytes(p: Problem) -> int:
+    """Bytes one decode step must move at least: the float32 state read and
+    written once, x, delta, (z) and y in the I/O dtype, B and C of the token,
+    A, D and dt_bias."""
+    e = 2 if p.dtype == "bf16" else 4
+    n = 2 * p.batch * p.dim * p.dstate * 4
+    n += p.batch * p.dim * e * (3 + (1 if p.z is not None else 0))
+    n += 2 * p.batch * p.dstate * e
+    n += p.dim * p.dstate * 4
+    n += p.dim * 4 * ((1 if p.D is not None else 0) + (1 if p.dt_bias is not None else 0))
+    return n

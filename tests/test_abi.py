@@ -3,6 +3,7 @@ header declares, and rejects bad arguments on the host before launching
 anything (every call below fails validation, so no kernel is launched and
 no fake pointer is ever dereferenced)."""
 import ctypes
+import glob
 import json
 import os
 import re
@@ -14,6 +15,7 @@ from selective_state_space_02_gb300 import _native, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 OK, ERR_NULL, ERR_DIMS, ERR_ALIGN, ERR_DTYPE, ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 ERR_ALIAS, ERR_VARIANT = -9, -10
@@ -26,14 +28,16 @@ def lib():
 
 
 def _declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(ssm_[a-z_0-9]+)\s*\(", src, re.M)))
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(ssm_[a-z_0-9]+)\s*\(", src, re.M))
+    return sorted(names)
 
 
 def test_header_declares_entry_points():
     names = _declared_functions()
-    assert "ssm_scan_fwd" in names and "ssm_scan_fwd_host" in names
+    assert "ssm_scan_fwd" in names and "ssm_scan_fwd_host" in names and "ssm_scan_step" in names
     assert set(names) == set(_native.SIGNATURES), "binding and header disagree"
 
 
@@ -43,8 +47,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_no_torch_in_the_abi():
-    src = open(HEADER).read()
-    assert "torch" not in src.lower().replace("pytorch", "") and "at::" not in src
+    for h in HEADERS:
+        src = open(h).read()
+        assert "torch" not in src.lower().replace("pytorch", "") and "at::" not in src
 
 
 def test_version_and_status_strings(lib):
@@ -169,3 +174,35 @@ def test_binding_type_checks():
         ssm.scan_fwd(x, x.bfloat16(), A, B, B)
     with pytest.raises(ValueError):
         ssm.scan_fwd(x, x, A, B, B)                          # CPU tensors on the device path
+
+
+def _from_state(lib, h0=16 * 65536, fs=None, y=16 * 32768, L=8, variant=0):
+    return lib.ssm_scan_fwd_from_state(16 * 2, 16 * 64, 16 * 4096, 16 * 8192, 16 * 16384, None, None, None, 1,
+                                       h0, y, fs, 1, 2, 4, L, 0, None, 0, None, variant)
+
+
+def test_from_state_validation(lib):
+    assert _from_state(lib, h0=16 * 65536 + 2) == ERR_ALIGN
+    assert _from_state(lib, h0=16 * 32768 + 4) == ERR_ALIAS             # start state inside y
+    assert _from_state(lib, h0=16 * 65536, fs=16 * 65536 + 8) == ERR_ALIAS   # partial overlap with final
+    assert _from_state(lib, h0=16 * 65536, fs=16 * 65536, L=0, variant=1) == OK   # in place, empty: no copy
+    assert _from_state(lib, variant=9) == ERR_VARIANT
+
+
+def _step(lib, state=16 * 65536, x=16 * 2, delta=16 * 64, A=16 * 4096, B=16 * 8192, C=16 * 16384, y=16 * 32768,
+          batch=1, dim=2, dstate=4, dtype=0):
+    return lib.ssm_scan_step(state, x, delta, A, B, C, None, None, None, 1, y, batch, dim, dstate, dtype, None)
+
+
+def test_step_validation(lib):
+    assert _step(lib, batch=0) == OK
+    assert _step(lib, state=None) == ERR_NULL
+    assert _step(lib, y=None) == ERR_NULL
+    assert _step(lib, dstate=0) == ERR_DIMS
+    assert _step(lib, dstate=65) == ERR_DIMS
+    assert _step(lib, dtype=5) == ERR_DTYPE
+    assert _step(lib, state=16 * 65536 + 2) == ERR_ALIGN
+    assert _step(lib, x=16 * 2 + 1, dtype=1) == ERR_ALIGN
+    assert _step(lib, y=16 * 2) == ERR_ALIAS                 # y over x
+    assert _step(lib, y=16 * 65536 + 4) == ERR_ALIAS         # y over the state
+    assert _step(lib, state=16 * 4096) == ERR_ALIAS          # state over A
