@@ -83,6 +83,8 @@ def _load():
             lib.ssm_oracle_step.argtypes = [_dp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, _fp, ctypes.c_int, _dp,
                                             ctypes.c_long, ctypes.c_long, ctypes.c_long]
             lib.ssm_oracle_step.restype = ctypes.c_int
+            lib.ssm_oracle_bwd.argtypes = [_fp] * 8 + [ctypes.c_int] + [_dp] * 12 + [ctypes.c_long] * 4
+            lib.ssm_oracle_bwd.restype = ctypes.c_int
             lib.ssm_oracle_pairs.argtypes = [_fp, _fp, _fp, _fp, _fp, ctypes.c_int,
                                              ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                              ctypes.c_long, ctypes.c_long, ctypes.c_long, _dp, _dp]
@@ -244,6 +246,43 @@ def step(state, x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=
     if rc != 0:
         raise RuntimeError(f"oracle step failed: {rc}")
     return h, y
+
+
+def bwd(x, delta, A, B, C, dy, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, dfinal=None):
+    """Gradients of the forward for a loss with dL/dy = dy [batch, dim, L]
+    and dL/dfinal_state = dfinal [batch, dim, dstate] (None: zero), fp64.
+    Returns a dict with dx, ddelta, dz (None without z), dA, dB, dC, dD,
+    ddt_bias and dh0 (float64 arrays in the shapes of the inputs)."""
+    x = _f32(x)
+    delta = _f32(delta)
+    A = _f32(A)
+    B = _f32(B)
+    C = _f32(C)
+    D = _f32(D)
+    z = _f32(z)
+    dt_bias = _f32(dt_bias)
+    batch, dim, L = x.shape
+    dstate = A.shape[1]
+    dy = _f64(dy)
+    assert dy.shape == x.shape
+    if h0 is not None:
+        h0 = _f64(h0)
+        assert h0.shape == (batch, dim, dstate)
+    if dfinal is not None:
+        dfinal = _f64(dfinal)
+        assert dfinal.shape == (batch, dim, dstate)
+    out = dict(dx=np.empty(x.shape), ddelta=np.empty(x.shape), dz=np.empty(x.shape) if z is not None else None,
+               dA=np.empty(A.shape), dB=np.empty(B.shape), dC=np.empty(C.shape), dD=np.empty((dim,)),
+               ddt_bias=np.empty((dim,)), dh0=np.empty((batch, dim, dstate)))
+    rc = _load().ssm_oracle_bwd(_ptr(x, _fp), _ptr(delta, _fp), _ptr(A, _fp), _ptr(B, _fp), _ptr(C, _fp),
+                                _ptr(D, _fp), _ptr(z, _fp), _ptr(dt_bias, _fp), int(bool(delta_softplus)),
+                                _ptr(h0, _dp), _ptr(dy, _dp), _ptr(dfinal, _dp),
+                                *[_ptr(out[k], _dp) for k in ("dx", "ddelta", "dA", "dB", "dC", "dD", "dz",
+                                                              "ddt_bias", "dh0")],
+                                batch, dim, dstate, L)
+    if rc != 0:
+        raise RuntimeError(f"oracle backward failed: {rc}")
+    return out
 
 
 def pairs(x, delta, A, B, dt_bias, delta_softplus, b, d, n):

@@ -337,6 +337,128 @@ int ssm_oracle_step(double *state, const float *x, const float *delta, const flo
     return 0;
 }
 
+/*
+ * Gradients of the forward above (reverse mode, written out from its
+ * definition) for a scalar loss whose derivatives with respect to y and to the
+ * final state are dy [batch, dim, L] and dfinal [batch, dim, dstate] (NULL:
+ * zero).  This is the backward that the recomputation strategy of [P3]
+ * sect. 4.2-4.3 evaluates: the forward states h_t are recomputed (here all of
+ * them, serially, per channel) and the adjoint of the state runs backwards,
+ *   lambda_t[n] = dq_t * C[b,n,t] + a_{t+1}[n] * lambda_{t+1}[n],
+ * with q_t = sum_n C h_t + D x_t, g_t = silu(z_t), y_t = q_t g_t and
+ * dq_t = dy_t g_t.  From lambda:
+ *   dC[b,n,t] += dq_t h_t[n]               dB[b,n,t] += lambda_t[n] u_t
+ *   du_t = sum_n lambda_t[n] B[b,n,t]      da_t[n] = lambda_t[n] h_{t-1}[n]
+ *   dA[d,n] += da_t[n] a_t[n] Delta_t      dDelta_t = sum_n da_t[n] a_t[n] A[d,n] + du_t x_t
+ *   dx_t = du_t Delta_t + dq_t D[d]        dD[d] += dq_t x_t
+ *   dz_t = dy_t q_t silu'(z_t)             ddelta_t = dDelta_t softplus'(v_t) (or dDelta_t)
+ *   ddt_bias[d] += ddelta_t                dh0[b,d,n] = a_0[n] lambda_0[n]
+ * with u_t = Delta_t x_t, v_t = delta_t + dt_bias[d], softplus' = sigmoid.
+ * B and C are shared by the channels of a batch and A, D, dt_bias by the
+ * batches, so dB, dC, dA, dD and ddt_bias are sums over channels or batches.
+ *
+ * Outputs (double, overwritten; NULL skips one): dx, ddelta, dz [batch, dim, L];
+ * dA [dim, dstate]; dB, dC [batch, dstate, L]; dD, ddt_bias [dim];
+ * dh0 [batch, dim, dstate].  Runs serially (the sums above are shared).
+ * Returns 0, or -1 on bad arguments or allocation failure.
+ */
+int ssm_oracle_bwd(const float *x, const float *delta, const float *A,
+                   const float *Bm, const float *Cm, const float *Dskip,
+                   const float *z, const float *dt_bias, int softplus,
+                   const double *h0, const double *dy, const double *dfinal,
+                   double *dx, double *ddelta, double *dA, double *dBm, double *dCm,
+                   double *dD, double *dz, double *ddt_bias, double *dh0,
+                   long batch, long dim, long dstate, long L)
+{
+    if (!x || !delta || !A || !Bm || !Cm || !dy) return -1;
+    if (batch <= 0 || dim <= 0 || dstate <= 0 || L < 0) return -1;
+    size_t nx = (size_t)batch * (size_t)dim * (size_t)L;
+    size_t nb = (size_t)batch * (size_t)dstate * (size_t)L;
+    if (dx) memset(dx, 0, nx * sizeof(double));
+    if (ddelta) memset(ddelta, 0, nx * sizeof(double));
+    if (dz) memset(dz, 0, nx * sizeof(double));
+    if (dA) memset(dA, 0, (size_t)dim * (size_t)dstate * sizeof(double));
+    if (dBm) memset(dBm, 0, nb * sizeof(double));
+    if (dCm) memset(dCm, 0, nb * sizeof(double));
+    if (dD) memset(dD, 0, (size_t)dim * sizeof(double));
+    if (ddt_bias) memset(ddt_bias, 0, (size_t)dim * sizeof(double));
+    size_t Lz = L > 0 ? (size_t)L : 1;
+    double *hs = (double *)malloc((Lz + 1) * (size_t)dstate * sizeof(double));   /* h_{-1} .. h_{L-1} */
+    double *Dl = (double *)malloc(Lz * sizeof(double));
+    double *vv = (double *)malloc(Lz * sizeof(double));
+    double *qq = (double *)malloc(Lz * sizeof(double));
+    double *lam = (double *)malloc((size_t)dstate * sizeof(double));
+    if (!hs || !Dl || !vv || !qq || !lam) {
+        free(hs); free(Dl); free(vv); free(qq); free(lam);
+        return -1;
+    }
+    for (long c = 0; c < batch * dim; ++c) {
+        long bb = c / dim, d = c % dim;
+        const float *xr = x + (size_t)c * (size_t)L;
+        const float *dr = delta + (size_t)c * (size_t)L;
+        const float *zr = z ? z + (size_t)c * (size_t)L : NULL;
+        const float *Br = Bm + (size_t)bb * (size_t)dstate * (size_t)L;
+        const float *Cr = Cm + (size_t)bb * (size_t)dstate * (size_t)L;
+        const float *Ar = A + (size_t)d * (size_t)dstate;
+        const double *dyr = dy + (size_t)c * (size_t)L;
+        double bias = dt_bias ? (double)dt_bias[d] : 0.0;
+        double Dd = Dskip ? (double)Dskip[d] : 0.0;
+        /* forward, keeping every state: row t+1 of hs holds h_t */
+        for (long n = 0; n < dstate; ++n) hs[n] = h0 ? h0[(size_t)c * (size_t)dstate + (size_t)n] : 0.0;
+        for (long t = 0; t < L; ++t) {
+            double xt = (double)xr[t];
+            vv[t] = (double)dr[t] + bias;
+            Dl[t] = softplus ? ssm_oracle_softplus(vv[t]) : vv[t];
+            double p = 0.0;
+            for (long n = 0; n < dstate; ++n) {
+                double at = exp(Dl[t] * (double)Ar[n]);
+                double prev = hs[(size_t)t * (size_t)dstate + (size_t)n];
+                double cur = at * prev + Dl[t] * xt * (double)Br[(size_t)n * (size_t)L + (size_t)t];
+                hs[(size_t)(t + 1) * (size_t)dstate + (size_t)n] = cur;
+                p += (double)Cr[(size_t)n * (size_t)L + (size_t)t] * cur;
+            }
+            qq[t] = p + Dd * xt;
+        }
+        /* reverse */
+        for (long n = 0; n < dstate; ++n) lam[n] = dfinal ? dfinal[(size_t)c * (size_t)dstate + (size_t)n] : 0.0;
+        for (long t = L - 1; t >= 0; --t) {
+            double xt = (double)xr[t];
+            double dq = dyr[t];
+            if (zr) {
+                double zt = (double)zr[t];
+                double sg = 1.0 / (1.0 + exp(-zt));
+                if (dz) dz[(size_t)c * (size_t)L + (size_t)t] = dyr[t] * qq[t] * (sg + zt * sg * (1.0 - sg));
+                dq = dyr[t] * zt * sg;
+            }
+            if (dD) dD[d] += dq * xt;
+            double du = 0.0, dDl = 0.0;
+            for (long n = 0; n < dstate; ++n) {
+                size_t bi = (size_t)bb * (size_t)dstate * (size_t)L + (size_t)n * (size_t)L + (size_t)t;
+                double ht = hs[(size_t)(t + 1) * (size_t)dstate + (size_t)n];
+                double hp = hs[(size_t)t * (size_t)dstate + (size_t)n];
+                lam[n] += dq * (double)Cr[(size_t)n * (size_t)L + (size_t)t];
+                if (dCm) dCm[bi] += dq * ht;
+                if (dBm) dBm[bi] += lam[n] * Dl[t] * xt;
+                du += lam[n] * (double)Br[(size_t)n * (size_t)L + (size_t)t];
+                double at = exp(Dl[t] * (double)Ar[n]);
+                double da = lam[n] * hp;
+                if (dA) dA[(size_t)d * (size_t)dstate + (size_t)n] += da * at * Dl[t];
+                dDl += da * at * (double)Ar[n];
+                lam[n] *= at;
+            }
+            dDl += du * xt;
+            if (dx) dx[(size_t)c * (size_t)L + (size_t)t] = du * Dl[t] + dq * Dd;
+            double dv = softplus ? dDl / (1.0 + exp(-vv[t])) : dDl;
+            if (ddelta) ddelta[(size_t)c * (size_t)L + (size_t)t] = dv;
+            if (ddt_bias) ddt_bias[d] += dv;
+        }
+        if (dh0)
+            for (long n = 0; n < dstate; ++n) dh0[(size_t)c * (size_t)dstate + (size_t)n] = lam[n];
+    }
+    free(hs); free(Dl); free(vv); free(qq); free(lam);
+    return 0;
+}
+
 /* The per-step pairs (a_t, b_t) of one recurrence (b, d, n), t = 0..L-1, as
  * defined in [P1 sect. 1.2]; used to feed the scan orderings above with the
  * exact pairs the forward recurrence consumes. */
