@@ -7,11 +7,13 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--variant auto|fused|chunked|twopass] [--impl ours|reference]
-                  [--op fwd|step]
+                  [--op fwd|step|bwd]
 
 ``--op step`` times the single-token decode step (ssm_scan_step) on the
 decode workload instead: one step = one token for every sequence of the
 batch, the state resident in HBM, reported against the HBM roofline.
+``--op bwd`` times the backward (ssm_scan_bwd: chunk-start states, then the
+reverse walk with chunk recomputation) on the forward workload.
 
 N > 1 runs under torch.distributed.run, one rank per GPU: every rank scans its
 own batch of the same shape (weak scaling, no data-path collective); the
@@ -70,7 +72,7 @@ def parse_args(argv=None):
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clock sampling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "step"])
+    ap.add_argument("--op", default="fwd", choices=["fwd", "step", "bwd"])
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -577,12 +579,148 @@ def run_step(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------ backward
+BWD_METRIC = "selective-scan backward Gelem/s (B·D·L/s)"
+
+
+def bwd_min_bytes(p) -> int:
+    """Bytes the backward must move at least: the forward's inputs (x, delta,
+    z, B, C in the I/O dtype; A, D, dt_bias) and dy read once; dx, ddelta,
+    dz written in the I/O dtype, dB and dC in float32, dA, dD, ddt_bias."""
+    e = 2 if p.dtype == "bf16" else 4
+    z = 1 if p.z is not None else 0
+    n = p.batch * p.dim * p.seqlen * e * ((3 + z) + (2 + z))   # x, delta, dy, (z) in; dx, ddelta, (dz) out
+    n += 2 * p.batch * p.dstate * p.seqlen * e + 2 * p.batch * p.dstate * p.seqlen * 4
+    n += 2 * p.dim * p.dstate * 4 + 4 * p.dim * 4
+    return n
+
+
+def run_bwd(args):
+    import torch
+    import numpy as np
+    import selective_state_space_02_gb300 as ssm
+    from selective_state_space_02_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    p, cfg = workload_problem(args.workload, rank)
+    g = lambda t: None if t is None else t.to(dev)
+    x, dl, z, B, C, A, D, bias = (g(p.x), g(p.delta), g(p.z), g(p.B), g(p.C), g(p.A), g(p.D), g(p.dt_bias))
+    dy = torch.from_numpy(np.random.default_rng(cfg["seed"] + 7).standard_normal(
+        (p.batch, p.dim, p.seqlen)).astype(np.float32)).to(p.torch_dtype)
+    ddy = dy.to(dev)
+    wsb = ssm._native.load().ssm_scan_bwd_workspace_size(p.batch, p.dim, p.dstate, p.seqlen,
+                                                          ssm._dtype_code(p.torch_dtype))
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return ssm.scan_bwd(x, dl, A, B, C, ddy, D=D, z=z, dt_bias=bias, delta_softplus=p.delta_softplus,
+                            workspace=ws)
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.time() + args.soak_s
+    while time.time() < t_end:
+        for _ in range(5):
+            flush_l2(flush)
+            step()
+        torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush_l2(flush)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    per = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(per), world, dev)
+    elems = p.elems
+    value = world * elems * args.steps / (total_ms / 1e3) / 1e9
+    hbm_peak, peak_kind = measured_peaks()
+    kern_s = statistics.mean(per) / 1e3
+    mb = bwd_min_bytes(p)
+    updates = elems * p.dstate
+    alu_peak = alu_peak_updates_per_s()
+    roofline = {"bound": "alu", "achieved": round(updates / kern_s / 1e12, 4), "peak": round(alu_peak / 1e12, 4),
+                "unit": "Tupdate/s", "frac": round(updates / kern_s / alu_peak, 4), "traffic": None,
+                "kernel": "backward (B/C re-layout, chunk totals, carry scan, reverse walk)",
+                "peak_basis": f"{SMS} SMs x {SM_MAX_MHZ:.0f} MHz x {UPDATES_PER_CLK_SM} (t,d,n) updates/clk/SM, "
+                              "one ex2 per update (the backward evaluates three: the totals pass, the chunk "
+                              "recomputation and the adjoint)",
+                "hbm": {"achieved": round(mb / kern_s / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                        "frac": round(mb / kern_s / 1e9 / hbm_peak, 4),
+                        "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                        "algorithmic_bytes_per_launch": mb}}
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: None if t is None else t.pin_memory()
+        hin = {"x": (pin(p.x), x), "delta": (pin(p.delta), dl), "z": (pin(p.z), z), "B": (pin(p.B), B),
+               "C": (pin(p.C), C), "dy": (pin(dy), ddy)}
+        hin = {k: v for k, v in hin.items() if v[0] is not None}
+        outs = {}
+
+        def hstep():
+            for hsrc, ddst in hin.values():
+                ddst.copy_(hsrc, non_blocking=True)
+            grads = step()
+            for k in ("dx", "ddelta", "dz", "dB", "dC"):
+                if grads.get(k) is not None:
+                    if k not in outs:
+                        outs[k] = torch.empty(grads[k].shape, dtype=grads[k].dtype).pin_memory()
+                    outs[k].copy_(grads[k], non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(args.warmup):
+            hstep()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            hstep()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": world * elems * args.steps / t_e2e / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": sum(v[0].numel() * v[0].element_size() for v in hin.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in outs.values()),
+               "api": "scan_bwd with its inputs copied from pinned host memory and the gradients copied back"}
+    line = {
+        "metric": BWD_METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": p.batch, "dim": p.dim, "dstate": p.dstate,
+                   "seqlen": p.seqlen, "io_dtype": p.dtype, "gate": p.z is not None,
+                   "l2": L2_NOTE.format(mib=args.flush_mib),
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "gpu_launches": args.steps * 4,   # B/C re-layout, chunk totals, carry scan, reverse walk
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "step":
         run_step(args)
+    elif args.op == "bwd":
+        run_bwd(args)
     else:
         run_ours(args)
 

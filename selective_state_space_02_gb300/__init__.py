@@ -14,7 +14,7 @@ import torch
 from . import _native
 from ._native import ScanError, VARIANTS, SSM_BF16, SSM_F32
 
-__all__ = ["scan_fwd", "scan_fwd_host", "scan_step", "select_variant", "workspace_size", "ScanError",
+__all__ = ["scan_fwd", "scan_fwd_host", "scan_step", "scan_bwd", "select_variant", "workspace_size", "ScanError",
            "VARIANTS", "host_buffer_size"]
 
 
@@ -211,3 +211,42 @@ def scan_step(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torc
                                       N, code, torch.cuda.current_stream(x.device).cuda_stream)
     _native.check(rc)
     return y
+
+
+def scan_bwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+             dy: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+             dt_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+             initial_state: Optional[torch.Tensor] = None, dfinal_state: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None) -> dict:
+    """Gradients of the forward (include/ssm_bwd.h) on CUDA tensors, for a
+    loss with dL/dy = dy (dtype of x) and dL/dfinal_state = dfinal_state
+    (float32, optional).  Returns a dict: dx, ddelta, dz (dtype of x; dz only
+    with z), dA, dB, dC, dD (only with D), ddt_bias (only with dt_bias) and
+    dinitial_state (float32)."""
+    batch, dim, N, L = _check_inputs(x, delta, A, B, C, D, z, dt_bias, "cuda")
+    if dy.dtype != x.dtype or dy.shape != x.shape or not dy.is_contiguous():
+        raise ValueError("dy must be a contiguous tensor like x")
+    for name, t in (("initial_state", initial_state), ("dfinal_state", dfinal_state)):
+        if t is not None and (t.dtype != torch.float32 or t.shape != (batch, dim, N) or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 [batch, dim, dstate] tensor")
+    lib = _native.load()
+    code = _dtype_code(x.dtype)
+    f32 = dict(dtype=torch.float32, device=x.device)
+    g = dict(dx=torch.empty_like(x), ddelta=torch.empty_like(x), dz=torch.empty_like(x) if z is not None else None,
+             dA=torch.empty((dim, N), **f32), dB=torch.empty((batch, N, L), **f32),
+             dC=torch.empty((batch, N, L), **f32), dD=torch.empty((dim,), **f32) if D is not None else None,
+             ddt_bias=torch.empty((dim,), **f32) if dt_bias is not None else None,
+             dinitial_state=torch.empty((batch, dim, N), **f32))
+    ws_bytes = lib.ssm_scan_bwd_workspace_size(batch, dim, N, L, code)
+    if ws_bytes == (1 << 64) - 1:
+        raise ScanError(-2, "invalid sizes")
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    rc = lib.ssm_scan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                          int(bool(delta_softplus)), _ptr(initial_state), _ptr(dy), _ptr(dfinal_state),
+                          _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                          _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dinitial_state"]),
+                          batch, dim, N, L, code, _ptr(workspace) if ws_bytes else None, ws_bytes,
+                          torch.cuda.current_stream(x.device).cuda_stream)
+    _native.check(rc)
+    return g

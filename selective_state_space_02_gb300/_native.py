@@ -41,6 +41,10 @@ SIGNATURES = {
     "ssm_scan_fwd_from_state": (_i, list(_FWD_ARGS[:9]) + [_vp] + list(_FWD_ARGS[9:]) + [_i]),
     # state, x, delta, A, B, C, D, z, dt_bias, softplus, y, batch, dim, dstate, dtype, stream
     "ssm_scan_step": (_i, [_vp] * 9 + [_i, _vp, _i, _i, _i, _i, _vp]),
+    "ssm_scan_bwd_workspace_size": (_sz, [_i, _i, _i, _i64, _i]),
+    # x, delta, A, B, C, D, z, dt_bias, softplus, h0, dy, dfinal, dx, ddelta, dA, dB, dC, dD, dz, ddt_bias,
+    # dh0, batch, dim, dstate, seqlen, dtype, workspace, bytes, stream
+    "ssm_scan_bwd": (_i, [_vp] * 8 + [_i] + [_vp] * 12 + [_i, _i, _i, _i64, _i, _vp, _sz, _vp]),
 }
 
 

@@ -272,6 +272,42 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
 
 unsigned int *device_status_word() { return status_ptr(); }
 
+size_t chunk_states_workspace_bytes(int batch, int dim, int dstate, int64_t L, int64_t seg_len) {
+    const int64_t nseg = L > 0 ? (L + seg_len - 1) / seg_len : 0;
+    const int64_t nchan = (int64_t)batch * dim;
+    size_t h = (size_t)nseg * nchan * dstate * sizeof(float);
+    size_t s = (size_t)nseg * nchan * sizeof(float);
+    return (h + 255) / 256 * 256 + (s + 255) / 256 * 256 + bc_bytes(batch, dstate, L);
+}
+
+cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspace, cudaStream_t st) {
+    // The first two steps of the two-pass forward with segments of seg_len
+    // steps: per-segment totals from the zero state, then the carry scan over
+    // the segments seeded with the start state.
+    const int nseg = (int)((a.L + seg_len - 1) / seg_len);
+    const int64_t nchan = (int64_t)a.batch * a.dim;
+    size_t hbytes = (size_t)nseg * nchan * a.dstate * sizeof(float);
+    hbytes = (hbytes + 255) / 256 * 256;
+    size_t sbytes = (size_t)nseg * nchan * sizeof(float);
+    sbytes = (sbytes + 255) / 256 * 256;
+    char *ws = static_cast<char *>(workspace);
+    fused::SegArgs sg{seg_len, nseg, reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes),
+                      reinterpret_cast<const float *>(ws + hbytes + sbytes)};
+    const int cfg = twopass_cfg(padded_states(a.dstate));
+    cudaError_t e = cudaSuccess;
+    if (nseg > 1) {
+        fused::SegArgs s1 = sg;
+        s1.nseg = nseg - 1;
+        e = launch_mode(a, s1, fused::kTotals, cfg, true, st);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t pairs = nchan * a.dstate;
+    const int wpb = 8;
+    segment_carry_kernel<<<(unsigned)((pairs + wpb - 1) / wpb), wpb * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, a.h0,
+                                                                                   nchan, a.dim, a.dstate, nseg);
+    return cudaGetLastError();
+}
+
 int read_device_status(cudaStream_t st, bool clear, unsigned int *out) {
     unsigned int *p = status_ptr();
     if (!p) return -1;

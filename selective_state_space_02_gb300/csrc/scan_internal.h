@@ -35,6 +35,13 @@ cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t s);
 cudaError_t launch_chunked(const FwdArgs &a, cudaStream_t s);
 cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t s);
 
+// States at the start of every segment of seg_len steps (segment 0 starts
+// from a.h0, or zero), as [nseg][batch*dim][dstate] float32 at the start of
+// `workspace`, computed by the two-pass forward's totals pass and carry scan.
+// The workspace also holds that pass's segment sums and prepared B/C rows.
+size_t chunk_states_workspace_bytes(int batch, int dim, int dstate, int64_t L, int64_t seg_len);
+cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspace, cudaStream_t st);
+
 // Device address of the status word of the bounded waits on the current
 // device (nullptr if the lookup fails); kernels OR bit 0 into it.
 unsigned int *device_status_word();

@@ -206,3 +206,25 @@ def test_step_validation(lib):
     assert _step(lib, y=16 * 2) == ERR_ALIAS                 # y over x
     assert _step(lib, y=16 * 65536 + 4) == ERR_ALIAS         # y over the state
     assert _step(lib, state=16 * 4096) == ERR_ALIAS          # state over A
+
+
+def _bwd(lib, dy=16 * 1024, dx=16 * 40000, ddelta=16 * 41000, dA=16 * 42000, dB=16 * 43000, dC=16 * 44000,
+         D=None, dD=None, z=None, dz=None, ws=None, wsb=0, L=8, dtype=0):
+    # fake, well-separated aligned addresses; every case fails validation before any launch
+    return lib.ssm_scan_bwd(16 * 2, 16 * 64, 16 * 4096, 16 * 8192, 16 * 16384, D, z, None, 1, None, dy, None,
+                            dx, ddelta, dA, dB, dC, dD, dz, None, None, 1, 2, 4, L, dtype, ws, wsb, None)
+
+
+def test_bwd_validation(lib):
+    assert lib.ssm_scan_bwd_workspace_size(1, 2, 4, 8, 0) > 0
+    assert lib.ssm_scan_bwd_workspace_size(1, 2, 4, 0, 0) == 0
+    assert lib.ssm_scan_bwd_workspace_size(1, 2, 65, 8, 0) == (1 << 64) - 1
+    assert _bwd(lib, dy=None) == ERR_NULL
+    assert _bwd(lib, dB=None) == ERR_NULL
+    assert _bwd(lib, D=16 * 50000) == ERR_NULL                  # D without dD
+    assert _bwd(lib, z=16 * 51000) == ERR_NULL                  # z without dz
+    assert _bwd(lib, dx=16 * 2) == ERR_ALIAS                    # dx over x
+    assert _bwd(lib, dC=16 * 43000 + 16) == ERR_ALIAS           # dC over dB
+    assert _bwd(lib, dA=16 * 42000 + 2) == ERR_ALIGN
+    assert _bwd(lib, dtype=7) == ERR_DTYPE
+    assert _bwd(lib) == ERR_WORKSPACE                           # workspace required
