@@ -16,14 +16,17 @@
 //         was processed, go to shared memory as Delta, u = Delta x,
 //         softplus'(v), dq = dy silu(z) and dy silu'(z);
 //      b. (serial, per lane) the chunk's states h_t = a_t h_{t-1} + u_t B_t,
-//         recomputed from its start state into shared memory;
-//      c. (serial, per lane) the state's adjoint backwards over the chunk,
-//         lambda <- lambda + dq C, stored, then lambda <- a lambda;
-//      d. (parallel) per lane, dA += sum_t lambda_t h_{t-1} a_t Delta_t; per
-//         (step, channel), the sums over the states of lambda B, of
-//         lambda h_{t-1} a A and of C h, which finish dx, ddelta and dz; per
-//         (step, state), dB and dC summed over the CTA's channels and added
-//         to global memory (one atomic addition per element per CTA);
+//         recomputed from its start state into registers, SC steps at a time
+//         (the last SC steps first; a sub-chunk's start state is advanced from
+//         the chunk's start again);
+//      c. (serial, per lane) the state's adjoint backwards over those steps,
+//         lambda <- lambda + dq C, then lambda <- a lambda, writing per step
+//         the lane's terms (lambda B, lambda h_{t-1} a A and C h summed over
+//         its states; lambda u and dq h per state) to shared memory;
+//      d. (parallel, every F steps) per (step, channel), the sums over the
+//         lanes' terms finish dx, ddelta and dz; per (step, state), dB and dC
+//         summed over the CTA's channels are added to global memory (one
+//         atomic addition per element per CTA); dA accumulates per lane;
 //    and at the end adds dA, dD and ddt_bias (shared by batches) and writes
 //    the start state's gradient.
 #include "../../include/ssm_bwd.h"
@@ -72,20 +75,25 @@ struct Shape {
     static constexpr int CPW = 32 / LPC;            // channels per warp
     static constexpr int CPC = kWarps * CPW;        // channels per CTA
     static constexpr int NT = kWarps * 32;
-    static constexpr int RW = NP + 1;               // padded row of a (step, channel) state vector
+    static constexpr int SC = 16;                   // steps whose states a lane keeps in registers
+    static constexpr int F = 8;                     // steps between reductions of the adjoint's terms
     // shared memory layout, in floats
-    static constexpr int per = CPC * kChunk;        // one value per (step, channel): index j * CPC + c
-    static constexpr int o_dl = 0, o_u = per, o_x = 2 * per, o_dq = 3 * per, o_sg = 4 * per, o_zp = 5 * per;
-    static constexpr int o_B = 6 * per;                       // [kChunk][NP]
-    static constexpr int o_C = o_B + kChunk * NP;
-    static constexpr int o_A = o_C + kChunk * NP;             // [CPC][NP]
-    static constexpr int o_H = o_A + CPC * NP;                // [kChunk + 1][CPC][RW]: row 0 = chunk start
-    static constexpr int o_G = o_H + (kChunk + 1) * CPC * RW; // [kChunk][CPC][RW]: the adjoint lambda_t
-    static constexpr size_t bytes = (size_t)(o_G + kChunk * CPC * RW) * 4;
+    static constexpr int IR = kChunk + 1;           // padded per-channel row of the step inputs
+    static constexpr int BR = NP + 1;               // padded B/C row (float2)
+    static constexpr int TR = CPC * NP + 1;         // padded dB/dC term block of one step (float2)
+    static constexpr int o_in = 0;                           // float4 [CPC][IR]: Delta, u, dq, x
+    static constexpr int o_sz = o_in + 4 * IR * CPC;         // float2 [CPC][IR]: softplus'(v), dy silu'(z)
+    static constexpr int o_bc = o_sz + 2 * IR * CPC;         // float2 [kChunk][BR]: B, C
+    static constexpr int o_ta = o_bc + 2 * kChunk * BR;      // float4 [F][CPC][LPC]: per-lane sums over its states
+    static constexpr int o_tb = o_ta + 4 * F * CPC * LPC;    // float2 [F][TR]: per-(channel, state) dB, dC terms
+    static constexpr size_t bytes = (size_t)(o_tb + 2 * F * TR) * 4;
     // per-thread shares of the cooperative loops
-    static constexpr int PER_T = per / NT;          // (step, channel) items per thread
-    static constexpr int BC_T = kChunk * NP / NT;   // (step, state) items per thread
-    static_assert(per % NT == 0 && (kChunk * NP) % NT == 0 && NT % CPC == 0, "thread split");
+    static constexpr int PER_T = CPC * kChunk / NT;           // (step, channel) items per thread
+    static constexpr int BC_T = kChunk * NP / NT;             // (step, state) items per thread
+    static constexpr int TA_T = (CPC * F + NT - 1) / NT;      // reduction over the states: (step, channel) items
+    static constexpr int TB_T = (F * NP + NT - 1) / NT;       // reduction over the channels: (step, state) items
+    static_assert((CPC * kChunk) % NT == 0 && (kChunk * NP) % NT == 0 && NT % CPC == 0, "thread split");
+    static_assert(kChunk % SC == 0 && SC % F == 0 && LPC >= 8, "sub-chunks and term buffers");
 };
 
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + ex2(-v * kLog2e)); }
@@ -105,8 +113,8 @@ __device__ __forceinline__ void load_raw(const BwdArgs &p, int b, int d0, int k,
     const int jn = (p.L - t0) < kChunk ? (int)(p.L - t0) : kChunk;
 #pragma unroll
     for (int i = 0; i < Sh::PER_T; ++i) {
-        const int e = threadIdx.x + i * Sh::NT;
-        const int c = e % Sh::CPC, j = e / Sh::CPC;
+        const int e = threadIdx.x + i * Sh::NT;          // consecutive threads: consecutive steps
+        const int c = e / kChunk, j = e % kChunk;
         const int dd = d0 + c;
         r.x[i] = r.v[i] = r.dy[i] = r.z[i] = 0.0f;
         if (dd < p.dim && j < jn) {
@@ -120,7 +128,7 @@ __device__ __forceinline__ void load_raw(const BwdArgs &p, int b, int d0, int k,
 #pragma unroll
     for (int i = 0; i < Sh::BC_T; ++i) {
         const int e = threadIdx.x + i * Sh::NT;
-        const int n = e % NP, j = e / NP;
+        const int n = e / kChunk, j = e % kChunk;
         r.B[i] = r.C[i] = 0.0f;
         if (n < p.N && j < jn) {
             const int64_t idx = ((int64_t)b * p.N + n) * p.L + t0 + j;
@@ -133,12 +141,18 @@ __device__ __forceinline__ void load_raw(const BwdArgs &p, int b, int d0, int k,
 template <typename T, int NP>
 __global__ void __launch_bounds__(kWarps * 32, 1) bwd_kernel(const BwdArgs p) {
     using Sh = Shape<NP>;
-    constexpr int LPC = Sh::LPC, S2 = Sh::S2, CPW = Sh::CPW, CPC = Sh::CPC, RW = Sh::RW, NT = Sh::NT;
+    constexpr int LPC = Sh::LPC, S2 = Sh::S2, CPW = Sh::CPW, CPC = Sh::CPC, NT = Sh::NT, F = Sh::F, SC = Sh::SC;
     extern __shared__ __align__(16) float sm[];
+    constexpr int IR = Sh::IR, BR = Sh::BR, TR = Sh::TR;
+    float4 *in = reinterpret_cast<float4 *>(sm + Sh::o_in);   // [CPC][IR]
+    float2 *sz = reinterpret_cast<float2 *>(sm + Sh::o_sz);   // [CPC][IR]
+    float2 *bc = reinterpret_cast<float2 *>(sm + Sh::o_bc);   // [kChunk][BR]
+    float4 *ta = reinterpret_cast<float4 *>(sm + Sh::o_ta);   // [F][CPC][LPC]
+    float2 *tb = reinterpret_cast<float2 *>(sm + Sh::o_tb);   // [F][TR]
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int li = lane % LPC;
-    const int c = warp * CPW + lane / LPC;          // the lane's channel within the CTA (lane phases)
+    const int c = warp * CPW + lane / LPC;          // the lane's channel within the CTA
     const int b = blockIdx.y;
     const int d0 = blockIdx.x * CPC;
     const int d = d0 + c;
@@ -149,147 +163,157 @@ __global__ void __launch_bounds__(kWarps * 32, 1) bwd_kernel(const BwdArgs p) {
     const int64_t chn = (int64_t)b * dim + d;
     const bool has_z = p.z != nullptr;
     const int nchunk = (int)((L + kChunk - 1) / kChunk);
-    const int tc = tid % CPC;                        // the thread's channel in the (step, channel) phases
-    const int td = d0 + tc;
-    const float tD = (td < dim && p.D) ? __ldg(p.D + td) : 0.0f;
+    // the (step, channel) reduction threads: step rj of each group of F steps
+    // (consecutive threads: consecutive steps), channel rc
+    const bool rthread = tid < CPC * F;
+    const int rj = tid % F, rc = tid / F, rd = d0 + rc;
+    const float rD = (rthread && rd < dim && p.D) ? __ldg(p.D + rd) : 0.0f;
 
-    float A2[S2], lam[S2], dAacc[S2];
+    float Av[S2], A2[S2], lam[S2], dAacc[S2];
 #pragma unroll
     for (int s = 0; s < S2; ++s) {
         const int n = li + LPC * s;
         const bool ok = dok && n < N;
-        const float Av = ok ? __ldg(p.A + (int64_t)d * N + n) : 0.0f;
-        A2[s] = Av * kLog2e;
+        Av[s] = ok ? __ldg(p.A + (int64_t)d * N + n) : 0.0f;
+        A2[s] = Av[s] * kLog2e;
         lam[s] = (ok && p.dfinal) ? p.dfinal[chn * N + n] : 0.0f;
         dAacc[s] = 0.0f;
     }
-    for (int e = tid; e < CPC * NP; e += NT) {
-        const int cc = e / NP, n = e % NP;
-        sm[Sh::o_A + e] = (d0 + cc < dim && n < N) ? __ldg(p.A + (int64_t)(d0 + cc) * N + n) : 0.0f;
-    }
-    float sum_dD = 0.0f, sum_db = 0.0f;              // this thread's share of dD, ddt_bias (channel tc)
+    float sum_dD = 0.0f, sum_db = 0.0f;              // this thread's share of dD, ddt_bias (channel rc)
 
     Raw<NP> raw;
     if (nchunk > 0) load_raw<T, NP>(p, b, d0, nchunk - 1, raw);
     for (int k = nchunk - 1; k >= 0; --k) {
         const int64_t t0 = (int64_t)k * kChunk;
         const int jn = (L - t0) < kChunk ? (int)(L - t0) : kChunk;
-        // ---- a. the chunk's inputs into shared memory ------------------------
+        // ---- a. the chunk's inputs (zero past the sequence and the channels) ----
 #pragma unroll
         for (int i = 0; i < Sh::PER_T; ++i) {
-            const int e = tid + i * NT;                     // = j * CPC + tc
+            const int e = tid + i * NT;                     // = channel * kChunk + j
             const float v = raw.v[i], xx = raw.x[i], g = raw.dy[i];
-            const float dl = p.softplus ? softplus2(make_float2(v, v)).x : v;
-            sm[Sh::o_dl + e] = dl;
-            sm[Sh::o_u + e] = dl * xx;
-            sm[Sh::o_x + e] = xx;
-            sm[Sh::o_sg + e] = p.softplus ? sigmoid_f(v) : 1.0f;
+            // past the sequence or the channels the step is the identity:
+            // Delta = 0 (softplus of the zero-filled input would be ln 2)
+            const bool valid = d0 + e / kChunk < dim && e % kChunk < jn;
+            const float dl = !valid ? 0.0f : p.softplus ? softplus2(make_float2(v, v)).x : v;
+            float dq = g, zp = 0.0f;
             if (has_z) {
                 const float zz = raw.z[i];
-                const float s = sigmoid_f(zz);
-                sm[Sh::o_dq + e] = g * zz * s;
-                sm[Sh::o_zp + e] = g * (s + zz * s * (1.0f - s));
-            } else {
-                sm[Sh::o_dq + e] = g;
+                const float sg = sigmoid_f(zz);
+                dq = g * zz * sg;
+                zp = g * (sg + zz * sg * (1.0f - sg));
             }
+            in[(e / kChunk) * IR + e % kChunk] = make_float4(dl, dl * xx, dq, xx);
+            sz[(e / kChunk) * IR + e % kChunk] = make_float2(p.softplus ? sigmoid_f(v) : 1.0f, zp);
         }
 #pragma unroll
         for (int i = 0; i < Sh::BC_T; ++i) {
-            const int e = tid + i * NT;                     // = j * NP + n
-            sm[Sh::o_B + e] = raw.B[i];
-            sm[Sh::o_C + e] = raw.C[i];
+            const int e = tid + i * NT;                     // = n * kChunk + j
+            bc[(e % kChunk) * BR + e / kChunk] = make_float2(raw.B[i], raw.C[i]);
         }
+        float hst[S2];                                      // the chunk's start state
 #pragma unroll
-        for (int s = 0; s < S2; ++s) {                      // the chunk's start state is row 0 of H
+        for (int s = 0; s < S2; ++s) {
             const int n = li + LPC * s;
-            sm[Sh::o_H + c * RW + n] = (dok && n < N) ? p.ws_h[((int64_t)k * nchan + chn) * N + n] : 0.0f;
+            hst[s] = (dok && n < N) ? p.ws_h[((int64_t)k * nchan + chn) * N + n] : 0.0f;
         }
         __syncthreads();
         if (k > 0) load_raw<T, NP>(p, b, d0, k - 1, raw);   // next chunk's inputs, in flight meanwhile
-        // ---- b. recompute the chunk's states (row j + 1 of H holds h_j) -----------
-        {
-            float h[S2];
+        // the chunk in sub-chunks of SC steps, last first: SC + 1 states per
+        // state fit in registers; a sub-chunk's start state is advanced from
+        // the chunk's start again
+        for (int sub = kChunk / SC - 1; sub >= 0; --sub) {
+            const int j0 = sub * SC;
+            float h[S2][SC + 1];                            // h[s][j + 1] = state after step j0 + j
 #pragma unroll
-            for (int s = 0; s < S2; ++s) h[s] = sm[Sh::o_H + c * RW + li + LPC * s];
-            for (int j = 0; j < jn; ++j) {
-                const float dl = sm[Sh::o_dl + j * CPC + c], u = sm[Sh::o_u + j * CPC + c];
-#pragma unroll
-                for (int s = 0; s < S2; ++s) {
-                    const int n = li + LPC * s;
-                    h[s] = fmaf(ex2(dl * A2[s]), h[s], u * sm[Sh::o_B + j * NP + n]);
-                    sm[Sh::o_H + ((j + 1) * CPC + c) * RW + n] = h[s];
-                }
-            }
-        }
-        // ---- c. the adjoint, backwards over the chunk: lambda_t into G ---------
-        for (int j = jn - 1; j >= 0; --j) {
-            const float dq = sm[Sh::o_dq + j * CPC + c], dl = sm[Sh::o_dl + j * CPC + c];
-#pragma unroll
-            for (int s = 0; s < S2; ++s) {
-                const int n = li + LPC * s;
-                lam[s] = fmaf(dq, sm[Sh::o_C + j * NP + n], lam[s]);
-                sm[Sh::o_G + (j * CPC + c) * RW + n] = lam[s];
-                lam[s] *= ex2(dl * A2[s]);
-            }
-        }
-        // ---- dA: sum over the chunk of lambda_t h_{t-1} a_t Delta_t ------------------
-        for (int j = 0; j < jn; ++j) {
-            const float dl = sm[Sh::o_dl + j * CPC + c];
-#pragma unroll
-            for (int s = 0; s < S2; ++s) {
-                const int n = li + LPC * s;
-                const float a = ex2(dl * A2[s]);
-                dAacc[s] = fmaf(sm[Sh::o_G + (j * CPC + c) * RW + n] * sm[Sh::o_H + (j * CPC + c) * RW + n] * a, dl,
-                                dAacc[s]);
-            }
-        }
-        __syncthreads();
-        // ---- d. per (step, channel): sums over the states; dx, ddelta, dz ---------
-#pragma unroll
-        for (int i = 0; i < Sh::PER_T; ++i) {
-            const int e = tid + i * NT;
-            const int j = e / CPC;
-            if (td < dim && j < jn) {
-                const float dl = sm[Sh::o_dl + e];
-                const float *g = sm + Sh::o_G + (j * CPC + tc) * RW;
-                const float *hp = sm + Sh::o_H + (j * CPC + tc) * RW;          // h_{t-1}
-                const float *hc = sm + Sh::o_H + ((j + 1) * CPC + tc) * RW;    // h_t
-                const float *Bj = sm + Sh::o_B + j * NP, *Cj = sm + Sh::o_C + j * NP, *Ac = sm + Sh::o_A + tc * NP;
-                float du = 0.0f, ds = 0.0f, pp = 0.0f;
-                for (int n = 0; n < N; ++n) {
-                    const float a = ex2(dl * Ac[n] * kLog2e);
-                    du = fmaf(g[n], Bj[n], du);
-                    ds = fmaf(g[n] * hp[n] * a, Ac[n], ds);
-                    pp = fmaf(Cj[n], hc[n], pp);
-                }
-                const float xx = sm[Sh::o_x + e], dq = sm[Sh::o_dq + e];
-                const float dv = (ds + du * xx) * sm[Sh::o_sg + e];
-                const int64_t idx = ((int64_t)b * dim + td) * L + t0 + j;
-                Io<T>::st(p.dx, idx, fmaf(du, dl, dq * tD));
-                Io<T>::st(p.ddelta, idx, dv);
-                if (has_z) Io<T>::st(p.dz, idx, sm[Sh::o_zp + e] * fmaf(tD, xx, pp));
-                sum_dD = fmaf(dq, xx, sum_dD);
-                sum_db += dv;
-            }
-        }
-        // ---- per (step, state): dB and dC summed over the CTA's channels ----------
-#pragma unroll
-        for (int i = 0; i < Sh::BC_T; ++i) {
-            const int e = tid + i * NT;
-            const int n = e % NP, j = e / NP;
-            if (n < N && j < jn) {
-                float db = 0.0f, dc = 0.0f;
+            for (int s = 0; s < S2; ++s) h[s][0] = hst[s];
 #pragma unroll 4
-                for (int cc = 0; cc < CPC; ++cc) {
-                    db = fmaf(sm[Sh::o_G + (j * CPC + cc) * RW + n], sm[Sh::o_u + j * CPC + cc], db);
-                    dc = fmaf(sm[Sh::o_dq + j * CPC + cc], sm[Sh::o_H + ((j + 1) * CPC + cc) * RW + n], dc);
+            for (int j = 0; j < j0; ++j) {
+                const float4 q = in[c * IR + j];
+#pragma unroll
+                for (int s = 0; s < S2; ++s)
+                    h[s][0] = fmaf(ex2(q.x * A2[s]), h[s][0], q.y * bc[j * BR + li + LPC * s].x);
+            }
+            // ---- b. recompute the sub-chunk's states into registers ----------
+#pragma unroll
+            for (int j = 0; j < SC; ++j) {
+                const float4 q = in[c * IR + j0 + j];
+#pragma unroll
+                for (int s = 0; s < S2; ++s)
+                    h[s][j + 1] = fmaf(ex2(q.x * A2[s]), h[s][j], q.y * bc[(j0 + j) * BR + li + LPC * s].x);
+            }
+            // ---- c. the adjoint backwards, F steps between reductions ----------
+#pragma unroll
+            for (int f = SC / F - 1; f >= 0; --f) {
+#pragma unroll
+                for (int jj = F - 1; jj >= 0; --jj) {
+                    const int jl = f * F + jj;                  // step within the sub-chunk
+                    const int j = j0 + jl;
+                    const float4 q = in[c * IR + j];
+                    float du = 0.0f, ds = 0.0f, pp = 0.0f;
+#pragma unroll
+                    for (int s = 0; s < S2; ++s) {
+                        const int n = li + LPC * s;
+                        const float2 BC = bc[j * BR + n];
+                        lam[s] = fmaf(q.z, BC.y, lam[s]);
+                        const float a = ex2(q.x * A2[s]);
+                        const float daa = lam[s] * h[s][jl] * a;     // (dL/da_t) a_t
+                        dAacc[s] = fmaf(daa, q.x, dAacc[s]);
+                        du = fmaf(lam[s], BC.x, du);
+                        ds = fmaf(daa, Av[s], ds);
+                        pp = fmaf(BC.y, h[s][jl + 1], pp);
+                        tb[jj * TR + c * NP + n] = make_float2(lam[s] * q.y, q.z * h[s][jl + 1]);
+                        lam[s] *= a;
+                    }
+                    ta[(jj * CPC + c) * LPC + li] = make_float4(du, ds, pp, 0.0f);
                 }
-                const int64_t idx = ((int64_t)b * N + n) * L + t0 + j;
-                atomicAdd(p.dB + idx, db);
-                atomicAdd(p.dC + idx, dc);
+                __syncthreads();
+                // sums over each channel's lanes: dx, ddelta, dz of (step, channel)
+                if (rthread) {
+                    const int j = j0 + f * F + rj;
+                    const float4 *row = ta + (rj * CPC + rc) * LPC;
+                    const int rot = tid & 7;                     // 8 lanes, 8 bank groups
+                    float du = 0.0f, ds = 0.0f, pp = 0.0f;
+#pragma unroll
+                    for (int m = 0; m < LPC; ++m) {
+                        const float4 t = row[(m + rot) & (LPC - 1)];
+                        du += t.x;
+                        ds += t.y;
+                        pp += t.z;
+                    }
+                    if (rd < dim && j < jn) {
+                        const float4 q = in[rc * IR + j];
+                        const float2 g = sz[rc * IR + j];
+                        const float dv = fmaf(du, q.w, ds) * g.x;
+                        const int64_t idx = ((int64_t)b * dim + rd) * L + t0 + j;
+                        Io<T>::st(p.dx, idx, fmaf(du, q.x, q.z * rD));
+                        Io<T>::st(p.ddelta, idx, dv);
+                        if (has_z) Io<T>::st(p.dz, idx, g.y * fmaf(rD, q.w, pp));
+                        sum_dD = fmaf(q.z, q.w, sum_dD);
+                        sum_db += dv;
+                    }
+                }
+                // sums over the CTA's channels: dB, dC of (step, state)
+#pragma unroll
+                for (int i = 0; i < Sh::TB_T; ++i) {
+                    const int e = tid + i * NT;          // consecutive threads: consecutive steps
+                    const int jj = e % F, n = e / F;
+                    const int j = j0 + f * F + jj;
+                    if (e < F * NP && n < N && j < jn) {
+                        float db = 0.0f, dc = 0.0f;
+#pragma unroll
+                        for (int cc = 0; cc < CPC; ++cc) {
+                            const float2 t = tb[jj * TR + cc * NP + n];
+                            db += t.x;
+                            dc += t.y;
+                        }
+                        const int64_t idx = ((int64_t)b * N + n) * L + t0 + j;
+                        atomicAdd(p.dB + idx, db);
+                        atomicAdd(p.dC + idx, dc);
+                    }
+                }
+                __syncthreads();   // the term buffers are refilled by the next group
             }
         }
-        __syncthreads();   // shared memory is refilled by the next chunk
     }
 #pragma unroll
     for (int s = 0; s < S2; ++s) {
@@ -299,9 +323,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) bwd_kernel(const BwdArgs p) {
             if (p.dh0) p.dh0[chn * N + n] = lam[s];
         }
     }
-    if (td < dim) {
-        if (p.dD) atomicAdd(p.dD + td, sum_dD);
-        if (p.ddt_bias) atomicAdd(p.ddt_bias + td, sum_db);
+    if (rthread && rd < dim) {
+        if (p.dD) atomicAdd(p.dD + rd, sum_dD);
+        if (p.ddt_bias) atomicAdd(p.ddt_bias + rd, sum_db);
     }
 }
 
