@@ -85,6 +85,8 @@ def _load():
             lib.ssm_oracle_step.restype = ctypes.c_int
             lib.ssm_oracle_bwd.argtypes = [_fp] * 8 + [ctypes.c_int] + [_dp] * 12 + [ctypes.c_long] * 4
             lib.ssm_oracle_bwd.restype = ctypes.c_int
+            lib.ssm_oracle_conv1d.argtypes = [_fp, _fp, _fp, _fp, ctypes.c_int, _dp, _dp] + [ctypes.c_long] * 4
+            lib.ssm_oracle_conv1d.restype = ctypes.c_int
             lib.ssm_oracle_pairs.argtypes = [_fp, _fp, _fp, _fp, _fp, ctypes.c_int,
                                              ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
                                              ctypes.c_long, ctypes.c_long, ctypes.c_long, _dp, _dp]
@@ -283,6 +285,27 @@ def bwd(x, delta, A, B, C, dy, D=None, z=None, dt_bias=None, delta_softplus=True
     if rc != 0:
         raise RuntimeError(f"oracle backward failed: {rc}")
     return out
+
+
+def conv1d(x, w, bias=None, state_in=None, silu=True):
+    """Causal depthwise convolution (K = w.shape[1] taps) with optional bias,
+    start history state_in [batch, dim, K-1] and SiLU, fp64.
+    Returns (y [batch, dim, L] float64, state_out [batch, dim, K-1] float64)."""
+    x = _f32(x)
+    w = _f32(w)
+    bias = _f32(bias)
+    state_in = _f32(state_in)
+    batch, dim, L = x.shape
+    K = w.shape[1]
+    assert w.shape == (dim, K) and (bias is None or bias.shape == (dim,))
+    assert state_in is None or state_in.shape == (batch, dim, K - 1)
+    y = np.empty((batch, dim, L))
+    st = np.empty((batch, dim, max(K - 1, 0)))
+    rc = _load().ssm_oracle_conv1d(_ptr(x, _fp), _ptr(w, _fp), _ptr(bias, _fp), _ptr(state_in, _fp), int(bool(silu)),
+                                   _ptr(y, _dp), _ptr(st, _dp), batch, dim, L, K)
+    if rc != 0:
+        raise RuntimeError(f"oracle conv1d failed: {rc}")
+    return y, st
 
 
 def pairs(x, delta, A, B, dt_bias, delta_softplus, b, d, n):

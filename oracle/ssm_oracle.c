@@ -459,6 +459,49 @@ int ssm_oracle_bwd(const float *x, const float *delta, const float *A,
     return 0;
 }
 
+/*
+ * Causal depthwise convolution in front of the scan ([P3] sect. 4.1 lists it
+ * among the operators the fused kernel runs before the scan): for every
+ * channel (b, d), with K taps w[d, 0..K-1],
+ *   v_t = bias[d] + sum_{k=0}^{K-1} w[d,k] * x[b,d,t-K+1+k]
+ *   y_t = silu(v_t) if `silu` else v_t
+ * where inputs before t = 0 come from state_in[b,d,0..K-2] (the K-1 inputs
+ * that preceded the sequence, oldest first; zeros if state_in is NULL).
+ * state_out[b,d,0..K-2] receives the last K-1 inputs of the history followed
+ * by the sequence, so that a following segment continues the convolution.
+ * Layouts: x [batch, dim, L] (float), w [dim, K], bias [dim] (optional),
+ * state_in [batch, dim, K-1] (float, optional), y [batch, dim, L] (double),
+ * state_out [batch, dim, K-1] (double, optional).  Returns 0, or -1 on bad
+ * arguments.
+ */
+int ssm_oracle_conv1d(const float *x, const float *w, const float *bias, const float *state_in, int silu,
+                      double *y, double *state_out, long batch, long dim, long L, long K)
+{
+    if (!x || !w || !y || batch < 0 || dim < 0 || L < 0 || K < 1 || K > 64) return -1;
+    double hist[64 + 1];
+    for (long c = 0; c < batch * dim; ++c) {
+        long d = c % dim;
+        const float *xr = x + (size_t)c * (size_t)L;
+        for (long k = 0; k < K - 1; ++k)
+            hist[k] = state_in ? (double)state_in[(size_t)c * (size_t)(K - 1) + (size_t)k] : 0.0;
+        for (long t = 0; t < L; ++t) {
+            double acc = bias ? (double)bias[d] : 0.0;
+            for (long k = 0; k < K; ++k) {
+                long src = t - (K - 1) + k;                      /* index into the sequence */
+                double xv = src >= 0 ? (double)xr[src] : hist[K - 1 + src];
+                acc += (double)w[(size_t)d * (size_t)K + (size_t)k] * xv;
+            }
+            y[(size_t)c * (size_t)L + (size_t)t] = silu ? ssm_oracle_silu(acc) : acc;
+        }
+        if (state_out)
+            for (long k = 0; k < K - 1; ++k) {
+                long src = L - (K - 1) + k;
+                state_out[(size_t)c * (size_t)(K - 1) + (size_t)k] = src >= 0 ? (double)xr[src] : hist[K - 1 + src];
+            }
+    }
+    return 0;
+}
+
 /* The per-step pairs (a_t, b_t) of one recurrence (b, d, n), t = 0..L-1, as
  * defined in [P1 sect. 1.2]; used to feed the scan orderings above with the
  * exact pairs the forward recurrence consumes. */

@@ -197,3 +197,22 @@ def step_min_bytes(p: Problem) -> int:
     n += p.dim * p.dstate * 4
     n += p.dim * 4 * ((1 if p.D is not None else 0) + (1 if p.dt_bias is not None else 0))
     return n
+
+
+def make_conv(dim: int, width: int = 4, seed: int = 0):
+    """Depthwise causal convolution parameters: weight [dim, width] and bias
+    [dim], float32, drawn U(-1/sqrt(width), 1/sqrt(width)) (the usual fan-in
+    scale for a depthwise filter of `width` taps)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = 1.0 / math.sqrt(width)
+    w = rng.uniform(-s, s, size=(dim, width)).astype(np.float32)
+    b = rng.uniform(-s, s, size=(dim,)).astype(np.float32)
+    return torch.from_numpy(w), torch.from_numpy(b)
+
+
+def make_conv_state(batch: int, dim: int, width: int = 4, dtype: str = "f32", seed: int = 0) -> torch.Tensor:
+    """The width-1 inputs that preceded a segment, [batch, dim, width-1], in the I/O dtype."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = rng.standard_normal((batch, dim, width - 1), dtype=np.float32)
+    t = torch.from_numpy(np.ascontiguousarray(s))
+    return t.to(torch.bfloat16) if dtype == "bf16" else t
