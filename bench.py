@@ -7,13 +7,16 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--variant auto|fused|chunked|twopass] [--impl ours|reference]
-                  [--op fwd|step|bwd]
+                  [--op fwd|step|bwd|conv]
 
 ``--op step`` times the single-token decode step (ssm_scan_step) on the
 decode workload instead: one step = one token for every sequence of the
 batch, the state resident in HBM, reported against the HBM roofline.
 ``--op bwd`` times the backward (ssm_scan_bwd: chunk-start states, then the
 reverse walk with chunk recomputation) on the forward workload.
+``--op conv`` times the causal depthwise convolution + SiLU in front of the
+scan (ssm_conv1d_fwd, 4 taps) on the forward workload's x, against the HBM
+roofline.
 
 N > 1 runs under torch.distributed.run, one rank per GPU: every rank scans its
 own batch of the same shape (weak scaling, no data-path collective); the
@@ -72,7 +75,7 @@ def parse_args(argv=None):
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clock sampling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "step", "bwd"])
+    ap.add_argument("--op", default="fwd", choices=["fwd", "step", "bwd", "conv"])
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -713,6 +716,109 @@ def run_bwd(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------- convolution
+CONV_METRIC = "causal depthwise conv1d + SiLU: Gelem/s (B·D·L/s) and achieved HBM GB/s as % of GB300 roofline"
+CONV_WIDTH = 4
+
+
+def run_conv(args):
+    import torch
+    import selective_state_space_02_gb300 as ssm
+    from selective_state_space_02_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    p, cfg = workload_problem(args.workload, rank)
+    x = p.x.to(dev)
+    w, b = synth.make_conv(p.dim, CONV_WIDTH, seed=cfg["seed"] + 11)
+    w, b = w.to(dev), b.to(dev)
+    y = torch.empty_like(x)
+    sout = torch.empty((p.batch, p.dim, CONV_WIDTH - 1), dtype=x.dtype, device=dev)
+    flush = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssm.conv1d(x, w, b, silu=True, y=y, state_out=sout)
+
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.time() + args.soak_s
+    while time.time() < t_end:
+        for _ in range(20):
+            flush_l2(flush)
+            step()
+        torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush_l2(flush)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    per = [a.elapsed_time(b_) for a, b_ in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(per), world, dev)
+    elems = p.elems
+    value = world * elems * args.steps / (total_ms / 1e3) / 1e9
+    hbm_peak, peak_kind = measured_peaks()
+    e = x.element_size()
+    mb = 2 * elems * e + p.dim * (CONV_WIDTH + 1) * 4 + p.batch * p.dim * (CONV_WIDTH - 1) * e
+    kern_s = statistics.mean(per) / 1e3
+    roofline = {"bound": "hbm", "achieved": round(mb / kern_s / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(mb / kern_s / 1e9 / hbm_peak, 4), "traffic": None,
+                "kernel": "conv1d (ssm_conv1d_fwd)", "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": mb}
+    e2e = None
+    if not args.no_e2e:
+        hx = p.x.pin_memory()
+        hy = torch.empty_like(hx).pin_memory()
+
+        def hstep():
+            x.copy_(hx, non_blocking=True)
+            step()
+            hy.copy_(y, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(args.warmup):
+            hstep()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            hstep()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": world * elems * args.steps / t_e2e / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": hx.numel() * hx.element_size(),
+               "d2h_bytes_per_step": hy.numel() * hy.element_size(),
+               "api": "conv1d with x copied from pinned host memory and y copied back"}
+    line = {
+        "metric": CONV_METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": p.batch, "dim": p.dim, "seqlen": p.seqlen,
+                   "width": CONV_WIDTH, "io_dtype": p.dtype, "silu": True,
+                   "l2": L2_NOTE.format(mib=args.flush_mib),
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -721,6 +827,8 @@ def main(argv=None):
         run_step(args)
     elif args.op == "bwd":
         run_bwd(args)
+    elif args.op == "conv":
+        run_conv(args)
     else:
         run_ours(args)
 

@@ -14,7 +14,7 @@ import torch
 from . import _native
 from ._native import ScanError, VARIANTS, SSM_BF16, SSM_F32
 
-__all__ = ["scan_fwd", "scan_fwd_host", "scan_step", "scan_bwd", "select_variant", "workspace_size", "ScanError",
+__all__ = ["scan_fwd", "scan_fwd_host", "scan_step", "scan_bwd", "conv1d", "select_variant", "workspace_size", "ScanError",
            "VARIANTS", "host_buffer_size"]
 
 
@@ -250,3 +250,37 @@ def scan_bwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
                           torch.cuda.current_stream(x.device).cuda_stream)
     _native.check(rc)
     return g
+
+
+def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+           state_in: Optional[torch.Tensor] = None, silu: bool = True, y: Optional[torch.Tensor] = None,
+           state_out: Optional[torch.Tensor] = None, return_state: bool = False):
+    """Causal depthwise convolution (+ SiLU) on CUDA tensors
+    (include/ssm_conv.h).  x: [batch, dim, L] float32 or bfloat16; weight:
+    [dim, width] and bias: [dim] float32; state_in / state_out: [batch, dim,
+    width-1] in the dtype of x.  Returns y, or (y, state_out) when
+    ``return_state``."""
+    code = _dtype_code(x.dtype)
+    if x.dim() != 3:
+        raise ValueError("x must be [batch, dim, seqlen]")
+    batch, dim, L = x.shape
+    if weight.dtype != torch.float32 or weight.dim() != 2 or weight.shape[0] != dim:
+        raise ValueError("weight must be float32 [dim, width]")
+    width = weight.shape[1]
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (dim,)):
+        raise ValueError("bias must be float32 [dim]")
+    for name, t in (("state_in", state_in), ("state_out", state_out)):
+        if t is not None and (t.dtype != x.dtype or t.shape != (batch, dim, width - 1)):
+            raise ValueError(f"{name} must be [batch, dim, width-1] in the dtype of x")
+    for name, t in (("x", x), ("weight", weight), ("bias", bias), ("state_in", state_in), ("state_out", state_out)):
+        if t is not None and (not t.is_contiguous() or t.device.type != "cuda"):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if y is None:
+        y = torch.empty_like(x)
+    if return_state and state_out is None:
+        state_out = torch.empty((batch, dim, width - 1), dtype=x.dtype, device=x.device)
+    rc = _native.load().ssm_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(state_in), _ptr(y),
+                                       _ptr(state_out), int(bool(silu)), batch, dim, L, width, code,
+                                       torch.cuda.current_stream(x.device).cuda_stream)
+    _native.check(rc)
+    return (y, state_out) if return_state else y

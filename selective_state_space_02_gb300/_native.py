@@ -41,6 +41,8 @@ SIGNATURES = {
     "ssm_scan_fwd_from_state": (_i, list(_FWD_ARGS[:9]) + [_vp] + list(_FWD_ARGS[9:]) + [_i]),
     # state, x, delta, A, B, C, D, z, dt_bias, softplus, y, batch, dim, dstate, dtype, stream
     "ssm_scan_step": (_i, [_vp] * 9 + [_i, _vp, _i, _i, _i, _i, _vp]),
+    # x, weight, bias, state_in, y, state_out, silu, batch, dim, seqlen, width, dtype, stream
+    "ssm_conv1d_fwd": (_i, [_vp] * 6 + [_i, _i, _i, _i64, _i, _i, _vp]),
     "ssm_scan_bwd_workspace_size": (_sz, [_i, _i, _i, _i64, _i]),
     # x, delta, A, B, C, D, z, dt_bias, softplus, h0, dy, dfinal, dx, ddelta, dA, dB, dC, dD, dz, ddt_bias,
     # dh0, batch, dim, dstate, seqlen, dtype, workspace, bytes, stream

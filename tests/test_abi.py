@@ -228,3 +228,19 @@ def test_bwd_validation(lib):
     assert _bwd(lib, dA=16 * 42000 + 2) == ERR_ALIGN
     assert _bwd(lib, dtype=7) == ERR_DTYPE
     assert _bwd(lib) == ERR_WORKSPACE                           # workspace required
+
+
+def _conv(lib, x=16 * 2, w=16 * 4096, b=None, sin=None, y=16 * 8192, sout=None, width=4, L=8, dtype=0):
+    # fake, well-separated aligned addresses; every case fails validation before any launch
+    return lib.ssm_conv1d_fwd(x, w, b, sin, y, sout, 1, 1, 2, L, width, dtype, None)
+
+
+def test_conv_validation(lib):
+    assert _conv(lib, width=0) == ERR_DIMS
+    assert _conv(lib, width=9) == ERR_DIMS
+    assert _conv(lib, dtype=3) == ERR_DTYPE
+    assert _conv(lib, x=None) == ERR_NULL
+    assert _conv(lib, w=None) == ERR_NULL
+    assert _conv(lib, x=16 * 2 + 1, dtype=1) == ERR_ALIGN
+    assert _conv(lib, y=16 * 2) == ERR_ALIAS                         # y over x
+    assert _conv(lib, sin=16 * 100, sout=16 * 100 + 4) == ERR_ALIAS   # state out over state in
