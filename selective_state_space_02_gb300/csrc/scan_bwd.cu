@@ -52,7 +52,8 @@ struct BwdArgs {
     int softplus;
     const float *ws_h;       // [nchunk][batch*dim][N] chunk-start states
     const void *dy;
-    const float *dfinal;     // nullable
+    const float *lam_in;     // nullable: [nseg][batch*dim][N] adjoint entering each segment from its right
+    int seg_chunks;          // chunks per segment (a CTA walks one segment)
     void *dx;
     void *ddelta;
     float *dA;
@@ -176,14 +177,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) bwd_kernel(const BwdArgs p) {
         const bool ok = dok && n < N;
         Av[s] = ok ? __ldg(p.A + (int64_t)d * N + n) : 0.0f;
         A2[s] = Av[s] * kLog2e;
-        lam[s] = (ok && p.dfinal) ? p.dfinal[chn * N + n] : 0.0f;
+        lam[s] = (ok && p.lam_in) ? p.lam_in[((int64_t)blockIdx.z * nchan + chn) * N + n] : 0.0f;
         dAacc[s] = 0.0f;
     }
     float sum_dD = 0.0f, sum_db = 0.0f;              // this thread's share of dD, ddt_bias (channel rc)
 
+    // this CTA's segment: chunks k_lo .. k_hi - 1
+    const int k_lo = blockIdx.z * p.seg_chunks;
+    const int k_hi = k_lo + p.seg_chunks < nchunk ? k_lo + p.seg_chunks : nchunk;
     Raw<NP> raw;
-    if (nchunk > 0) load_raw<T, NP>(p, b, d0, nchunk - 1, raw);
-    for (int k = nchunk - 1; k >= 0; --k) {
+    if (k_hi > k_lo) load_raw<T, NP>(p, b, d0, k_hi - 1, raw);
+    for (int k = k_hi - 1; k >= k_lo; --k) {
         const int64_t t0 = (int64_t)k * kChunk;
         const int jn = (L - t0) < kChunk ? (int)(L - t0) : kChunk;
         // ---- a. the chunk's inputs (zero past the sequence and the channels) ----
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) bwd_kernel(const BwdArgs p) {
             hst[s] = (dok && n < N) ? p.ws_h[((int64_t)k * nchan + chn) * N + n] : 0.0f;
         }
         __syncthreads();
-        if (k > 0) load_raw<T, NP>(p, b, d0, k - 1, raw);   // next chunk's inputs, in flight meanwhile
+        if (k > k_lo) load_raw<T, NP>(p, b, d0, k - 1, raw);   // next chunk's inputs, in flight meanwhile
         // the chunk in sub-chunks of SC steps, last first: SC + 1 states per
         // state fit in registers; a sub-chunk's start state is advanced from
         // the chunk's start again
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) bwd_kernel(const BwdArgs p) {
         const int n = li + LPC * s;
         if (dok && n < N) {
             atomicAdd(p.dA + (int64_t)d * N + n, dAacc[s]);
-            if (p.dh0) p.dh0[chn * N + n] = lam[s];
+            if (p.dh0 && blockIdx.z == 0) p.dh0[chn * N + n] = lam[s];   // the adjoint of the start state
         }
     }
     if (rthread && rd < dim) {
@@ -329,23 +333,173 @@ __global__ void __launch_bounds__(kWarps * 32, 1) bwd_kernel(const BwdArgs p) {
     }
 }
 
+// The adjoint's affine map over one segment of chunks: walking the segment's
+// steps backwards from lambda = 0 gives Q (lambda <- (lambda + dq C) a per
+// step), and the segment's sum of Delta gives P = exp(A sum Delta), so that
+// the adjoint leaving the segment on its left is P lambda_in + Q.  Same
+// lanes, chunk loads and Delta as bwd_kernel; no state is needed.
 template <typename T, int NP>
-cudaError_t launch_np(const BwdArgs &a, cudaStream_t st) {
+__global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArgs p, float *q_out, float *s_out) {
     using Sh = Shape<NP>;
+    constexpr int LPC = Sh::LPC, S2 = Sh::S2, CPW = Sh::CPW, CPC = Sh::CPC, NT = Sh::NT, IR = Sh::IR, BR = Sh::BR;
+    extern __shared__ __align__(16) float sm[];
+    float2 *dd = reinterpret_cast<float2 *>(sm);            // [CPC][IR]: Delta, dq
+    float *cs = sm + 2 * CPC * IR;                          // [kChunk][BR]: C
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int li = lane % LPC;
+    const int c = warp * CPW + lane / LPC;
+    const int b = blockIdx.y;
+    const int d0 = blockIdx.x * CPC;
+    const int d = d0 + c;
+    const int dim = p.dim, N = p.N;
+    const bool dok = d < dim;
+    const int64_t L = p.L;
+    const int64_t nchan = (int64_t)p.batch * dim;
+    const int64_t chn = (int64_t)b * dim + d;
+    const bool has_z = p.z != nullptr;
+    const int nchunk = (int)((L + kChunk - 1) / kChunk);
+    const int k_lo = blockIdx.z * p.seg_chunks;
+    const int k_hi = k_lo + p.seg_chunks < nchunk ? k_lo + p.seg_chunks : nchunk;
+    float A2[S2], lam[S2];
+#pragma unroll
+    for (int s = 0; s < S2; ++s) {
+        const int n = li + LPC * s;
+        A2[s] = (dok && n < N) ? __ldg(p.A + (int64_t)d * N + n) * kLog2e : 0.0f;
+        lam[s] = 0.0f;
+    }
+    float ssum = 0.0f;
+    Raw<NP> raw;
+    if (k_hi > k_lo) load_raw<T, NP>(p, b, d0, k_hi - 1, raw);
+    for (int k = k_hi - 1; k >= k_lo; --k) {
+        const int jn = (L - (int64_t)k * kChunk) < kChunk ? (int)(L - (int64_t)k * kChunk) : kChunk;
+#pragma unroll
+        for (int i = 0; i < Sh::PER_T; ++i) {
+            const int e = tid + i * NT;                     // = channel * kChunk + j
+            const bool valid = d0 + e / kChunk < dim && e % kChunk < jn;
+            const float v = raw.v[i], g = raw.dy[i];
+            const float dl = !valid ? 0.0f : p.softplus ? softplus2(make_float2(v, v)).x : v;
+            float dq = g;
+            if (has_z) {
+                const float zz = raw.z[i];
+                dq = g * zz * sigmoid_f(zz);
+            }
+            dd[(e / kChunk) * IR + e % kChunk] = make_float2(dl, dq);
+        }
+#pragma unroll
+        for (int i = 0; i < Sh::BC_T; ++i) {
+            const int e = tid + i * NT;                     // = n * kChunk + j
+            cs[(e % kChunk) * BR + e / kChunk] = raw.C[i];
+        }
+        __syncthreads();
+        if (k > k_lo) load_raw<T, NP>(p, b, d0, k - 1, raw);
+#pragma unroll 4
+        for (int j = kChunk - 1; j >= 0; --j) {
+            const float2 q = dd[c * IR + j];
+#pragma unroll
+            for (int s = 0; s < S2; ++s)
+                lam[s] = fmaf(q.y, cs[j * BR + li + LPC * s], lam[s]) * ex2(q.x * A2[s]);
+            ssum += q.x;
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int s = 0; s < S2; ++s) {
+        const int n = li + LPC * s;
+        if (dok && n < N) q_out[((int64_t)blockIdx.z * nchan + chn) * N + n] = lam[s];
+    }
+    if (dok && li == 0) s_out[(int64_t)blockIdx.z * nchan + chn] = ssum;
+}
+
+// The adjoint entering every segment from its right: starting from dfinal at
+// the end of the sequence, lambda <- exp(A sum Delta_s) lambda + Q_s from the
+// last segment to the first (the sum of Delta is the log-domain decay of the
+// segment).  ws_q holds Q_s on entry and the entering adjoint on return.
+__global__ void adj_carry_kernel(const float *__restrict__ A, const float *__restrict__ dfinal, float *ws_q,
+                                 const float *__restrict__ ws_s, int64_t nchan, int dim, int N, int nseg) {
+    const int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (pair >= nchan * N) return;
+    const int64_t ch = pair / N;
+    const int n = (int)(pair % N);
+    const float a2 = A[(ch % dim) * N + n] * kLog2e;
+    float lam = dfinal ? dfinal[ch * N + n] : 0.0f;
+    for (int z = nseg - 1; z >= 0; --z) {
+        const int64_t i = ((int64_t)z * nchan + ch) * N + n;
+        const float q = ws_q[i];
+        ws_q[i] = lam;
+        lam = fmaf(ex2(a2 * ws_s[(int64_t)z * nchan + ch]), lam, q);
+    }
+}
+
+// Segments of chunks: one CTA walks one segment.  Problems whose channels
+// fill a wave (3 CTAs per SM fit at once) keep one segment -- there the walk
+// is bound by the SMs' throughput and the totals pass would be pure cost.
+// Fewer channels get segments enough for about four waves (measured best on
+// the long-sequence shape: shorter serial walks, and the totals pass walks
+// shorter segments too); the adjoint entering each segment then comes from the
+// segment totals and the reverse carry.
+constexpr int64_t kWaveCtas = 152 * 3;
+constexpr int64_t kTargetCtas = 4 * kWaveCtas;
+
+int padded_np(int dstate) { return dstate <= 8 ? 8 : dstate <= 16 ? 16 : dstate <= 32 ? 32 : 64; }
+int cta_channels(int np) { return kWarps * (32 / (np < 32 ? np : 32)); }
+
+struct Plan {
+    int seg_chunks;   // chunks per segment
+    int nseg;         // segments
+};
+
+Plan plan_for(int batch, int dim, int dstate, int64_t L) {
+    const int nchunk = (int)((L + kChunk - 1) / kChunk);
+    const int cpc = cta_channels(padded_np(dstate));
+    const int64_t ncta = (int64_t)batch * ((dim + cpc - 1) / cpc);
+    if (nchunk <= 1 || ncta >= kWaveCtas) return Plan{nchunk > 0 ? nchunk : 1, 1};
+    const int64_t want = (kTargetCtas + ncta - 1) / ncta;
+    const int seg = (int)((nchunk + want - 1) / want);
+    return Plan{seg, (nchunk + seg - 1) / seg};
+}
+
+size_t r256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Bytes of the segment totals (adjoint Q, then the entering adjoint; sum of Delta).
+size_t seg_bytes(const Plan &pl, int64_t nchan, int dstate) {
+    if (pl.nseg <= 1) return 0;
+    return r256((size_t)pl.nseg * nchan * dstate * 4) + r256((size_t)pl.nseg * nchan * 4);
+}
+
+template <typename T, int NP>
+cudaError_t launch_np(BwdArgs a, const Plan &pl, const float *dfinal, char *seg_ws, cudaStream_t st) {
+    using Sh = Shape<NP>;
+    const unsigned gx = (unsigned)((a.dim + Sh::CPC - 1) / Sh::CPC);
+    a.seg_chunks = pl.seg_chunks;
+    a.lam_in = dfinal;
+    cudaError_t e;
+    if (pl.nseg > 1) {
+        const int64_t nchan = (int64_t)a.batch * a.dim;
+        float *q = reinterpret_cast<float *>(seg_ws);
+        float *ssum = reinterpret_cast<float *>(seg_ws + r256((size_t)pl.nseg * nchan * a.N * 4));
+        const size_t tb = (size_t)(2 * Sh::CPC * Sh::IR + kChunk * Sh::BR) * 4;
+        adj_totals_kernel<T, NP><<<dim3(gx, (unsigned)a.batch, (unsigned)pl.nseg), kWarps * 32, tb, st>>>(a, q, ssum);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const int64_t pairs = nchan * a.N;
+        adj_carry_kernel<<<(unsigned)((pairs + 255) / 256), 256, 0, st>>>(a.A, dfinal, q, ssum, nchan, a.dim, a.N,
+                                                                          pl.nseg);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        a.lam_in = q;
+    }
     auto kern = bwd_kernel<T, NP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::bytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((a.dim + Sh::CPC - 1) / Sh::CPC), (unsigned)a.batch);
-    kern<<<grid, kWarps * 32, Sh::bytes, st>>>(a);
+    kern<<<dim3(gx, (unsigned)a.batch, (unsigned)pl.nseg), kWarps * 32, Sh::bytes, st>>>(a);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_t(const BwdArgs &a, cudaStream_t st) {
-    if (a.N <= 8) return launch_np<T, 8>(a, st);
-    if (a.N <= 16) return launch_np<T, 16>(a, st);
-    if (a.N <= 32) return launch_np<T, 32>(a, st);
-    return launch_np<T, 64>(a, st);
+cudaError_t launch_t(const BwdArgs &a, const Plan &pl, const float *dfinal, char *seg_ws, cudaStream_t st) {
+    if (a.N <= 8) return launch_np<T, 8>(a, pl, dfinal, seg_ws, st);
+    if (a.N <= 16) return launch_np<T, 16>(a, pl, dfinal, seg_ws, st);
+    if (a.N <= 32) return launch_np<T, 32>(a, pl, dfinal, seg_ws, st);
+    return launch_np<T, 64>(a, pl, dfinal, seg_ws, st);
 }
 
 bool aligned(const void *q, size_t n) { return (reinterpret_cast<uintptr_t>(q) % n) == 0; }
@@ -366,7 +520,9 @@ extern "C" size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, in
     if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return (size_t)-1;
     if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64 || seqlen < 0) return (size_t)-1;
     if (batch == 0 || dim == 0 || seqlen == 0) return 0;
-    return ssm::chunk_states_workspace_bytes(batch, dim, dstate, seqlen, ssm::kChunk);
+    const ssm::Plan pl = ssm::plan_for(batch, dim, dstate, seqlen);
+    return ssm::r256(ssm::chunk_states_workspace_bytes(batch, dim, dstate, seqlen, ssm::kChunk)) +
+           ssm::seg_bytes(pl, (int64_t)batch * dim, dstate);
 }
 
 extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, const void *B, const void *C,
@@ -435,9 +591,13 @@ extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, co
         if (!aligned(q, 16)) v16 = false;
     f.vec16 = v16 ? 1 : 0;
     if (chunk_start_states(f, kChunk, workspace, st) != cudaSuccess) return SSM_ERR_LAUNCH;
+    const Plan pl = plan_for(batch, dim, dstate, seqlen);
+    char *seg_ws = static_cast<char *>(workspace) +
+                   r256(chunk_states_workspace_bytes(batch, dim, dstate, seqlen, kChunk));
     BwdArgs a{x, delta, A, B, C, D, z, dt_bias, delta_softplus ? 1 : 0, static_cast<const float *>(workspace),
-              dy, dfinal_state, dx, ddelta, dA, dB, dC, D ? dD : nullptr, z ? dz : nullptr, ddt_bias,
+              dy, nullptr, 1, dx, ddelta, dA, dB, dC, D ? dD : nullptr, z ? dz : nullptr, ddt_bias,
               dinitial_state, batch, dim, dstate, seqlen};
-    const cudaError_t e = io_dtype == SSM_BF16 ? launch_t<__nv_bfloat16>(a, st) : launch_t<float>(a, st);
+    const cudaError_t e = io_dtype == SSM_BF16 ? launch_t<__nv_bfloat16>(a, pl, dfinal_state, seg_ws, st)
+                                               : launch_t<float>(a, pl, dfinal_state, seg_ws, st);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
