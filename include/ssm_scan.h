@@ -178,8 +178,9 @@ int ssm_scan_fwd_from_state(const void *x, const void *delta, const float *A, co
 int ssm_scan_device_status(void *stream, int clear);
 
 /* Device bytes that ssm_scan_fwd_host needs as `device_buffer`: room for the
- * device copies of every input and output plus the variant's workspace,
- * each 256-byte aligned.  Returns (size_t)-1 for invalid sizes. */
+ * device copies of every input and output, the state carried between time
+ * chunks and the largest workspace a chunk needs, each 256-byte aligned.
+ * Returns (size_t)-1 for invalid sizes. */
 size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seqlen,
                                      int io_dtype, int has_D, int has_z, int has_dt_bias,
                                      int has_final_state, int variant);
@@ -187,11 +188,21 @@ size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seq
 /*
  * Forward selective scan on HOST buffers: the end-to-end call.  Same
  * arguments and layouts as ssm_scan_fwd, but every tensor pointer is a host
- * pointer (page-locked memory gives the fastest copies).  The inputs are
- * copied into `device_buffer` (caller-owned device memory of at least
- * ssm_scan_fwd_host_buffer_size() bytes, 256-byte aligned) with one
- * cudaMemcpyAsync each, the scan runs on `stream`, y and final_state are
- * copied back, and the call returns after `stream` has finished them.
+ * pointer (page-locked memory gives the fastest copies); `device_buffer` is
+ * caller-owned device memory of at least ssm_scan_fwd_host_buffer_size()
+ * bytes, 256-byte aligned.
+ *
+ * Problems of 16 MiB or more (x, delta, z and y together) are cut along the
+ * sequence into two time chunks, from 48 MiB into three.  Chunk j's columns of
+ * x, delta, z, B and C are copied in on an internal stream, scanned on
+ * `stream` starting from the state chunk j-1 ended in (ssm_scan_fwd_from_state
+ * semantics, the state kept in float32 on the device), and y's columns are
+ * copied back on a second internal stream, so the copies of neighbouring
+ * chunks overlap the scans; `variant` applies to every chunk (AUTO picks per
+ * chunk shape).  The internal streams and events are created by the first
+ * call on a device and kept until the process exits; calls on one device
+ * are serialised.  Work already queued on `stream` runs first, and the call
+ * returns after every copy has finished, also on error.
  */
 int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const void *B,
                       const void *C, const float *D, const void *z, const float *dt_bias,

@@ -4,6 +4,7 @@
 #include "scan_internal.h"
 
 #include <cstring>
+#include <mutex>
 
 namespace {
 
@@ -85,6 +86,75 @@ size_t workspace_for(int batch, int dim, int dstate, int64_t seqlen, int variant
 }
 
 size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Time chunks of the host-buffer entry point.  The inputs are copied, scanned
+// and copied back chunk after chunk on three streams, so that the copies of
+// chunk j+1 overlap the scan of chunk j and the copy back of chunk j-1; each
+// chunk starts from the state the previous one ended in.  Measured on GB300
+// (pinned memory, about 200 GB/s each way alone and 150 GB/s each way
+// together), three chunks gave the shortest calls on the 100 MB - 1.2 GB
+// problems: fewer leave the scan and the copy back exposed, more let the copy
+// back slow the copy in for longer and add per-chunk overhead.  Problems of
+// 48 MiB or more (x, delta, z and y) run in three chunks, from 16 MiB in two,
+// smaller ones in one; every chunk but the last is a whole number of 64-step
+// tiles (16-byte aligned rows in either dtype).
+constexpr int kMaxHostChunks = 3;
+
+struct HostPlan {
+    int64_t len;    // steps per chunk
+    int64_t last;   // steps of the last chunk
+    int n;          // number of chunks
+};
+
+HostPlan host_plan(int batch, int dim, int64_t seqlen, int io_dtype, bool has_z) {
+    const size_t bytes = (size_t)batch * dim * (size_t)seqlen * elem_size(io_dtype) * (has_z ? 4 : 3);
+    const int64_t k = bytes >= ((size_t)48 << 20) ? 3 : bytes >= ((size_t)16 << 20) ? 2 : 1;
+    int64_t len = k > 1 ? (seqlen + k - 1) / k : seqlen;
+    len = (len + 63) / 64 * 64;
+    if (len >= seqlen) return HostPlan{seqlen, seqlen, 1};
+    const int n = (int)((seqlen + len - 1) / len);
+    return HostPlan{len, seqlen - (int64_t)(n - 1) * len, n};
+}
+
+// Copy streams and events of one device for the host-buffer entry point,
+// created by its first call on that device and kept until the process exits.
+// The mutex serialises calls on the device, which share them.
+struct HostStreams {
+    std::mutex mu;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t ready[kMaxHostChunks] = {};
+    cudaEvent_t done[kMaxHostChunks] = {};
+};
+
+HostStreams *host_streams() {
+    static std::mutex mu;
+    static HostStreams *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev]) return cache[dev];
+    HostStreams *h = new HostStreams();
+    bool ok = cudaStreamCreateWithFlags(&h->in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h->out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kMaxHostChunks; ++i)
+        ok = cudaEventCreateWithFlags(&h->ready[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        if (h->in) cudaStreamDestroy(h->in);
+        if (h->out) cudaStreamDestroy(h->out);
+        if (h->start) cudaEventDestroy(h->start);
+        for (int i = 0; i < kMaxHostChunks; ++i) {
+            if (h->ready[i]) cudaEventDestroy(h->ready[i]);
+            if (h->done[i]) cudaEventDestroy(h->done[i]);
+        }
+        delete h;
+        return nullptr;
+    }
+    cache[dev] = h;
+    return h;
+}
 
 }  // namespace
 
@@ -221,8 +291,18 @@ int ssm_scan_device_status(void *stream, int clear) {
 size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                                      int has_D, int has_z, int has_dt_bias, int has_final_state,
                                      int variant) {
-    const size_t ws = ssm_scan_fwd_workspace_size(batch, dim, dstate, seqlen, io_dtype, variant);
-    if (ws == (size_t)-1) return (size_t)-1;
+    (void)has_final_state;   // the chunk-to-chunk state buffer is always present
+    if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return (size_t)-1;
+    if (!valid_sizes(batch, dim, dstate, seqlen)) return (size_t)-1;
+    if (resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant) < 0) return (size_t)-1;
+    const HostPlan hp = host_plan(batch, dim, seqlen, io_dtype, has_z != 0);
+    size_t ws = 0;
+    for (const int64_t len : {hp.len, hp.last}) {
+        const int v = resolve_variant(batch, dim, dstate, len, io_dtype, variant);
+        if (v < 0) return (size_t)-1;
+        const size_t w = workspace_for(batch, dim, dstate, len, v);
+        ws = w > ws ? w : ws;
+    }
     const size_t es = elem_size(io_dtype);
     const size_t nx = (size_t)batch * dim * (size_t)seqlen * es;
     const size_t nb = (size_t)batch * dstate * (size_t)seqlen * es;
@@ -232,7 +312,7 @@ size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seq
     total += round256((size_t)dim * dstate * 4);                    // A
     total += has_D ? round256((size_t)dim * 4) : 0;
     total += has_dt_bias ? round256((size_t)dim * 4) : 0;
-    total += has_final_state ? round256((size_t)batch * dim * dstate * 4) : 0;
+    total += round256((size_t)batch * dim * dstate * 4);            // state carried from chunk to chunk
     return total;
 }
 
@@ -244,43 +324,96 @@ int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const vo
     int rc = validate(x, delta, A, B, C, D, z, dt_bias, y, final_state, batch, dim, dstate, seqlen,
                       io_dtype);
     if (rc != SSM_OK) return rc;
-    const int v = resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant);
-    if (v < 0) return v;
+    if (resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant) < 0) return SSM_ERR_VARIANT;
     const size_t need = ssm_scan_fwd_host_buffer_size(batch, dim, dstate, seqlen, io_dtype, D != nullptr,
                                                       z != nullptr, dt_bias != nullptr,
-                                                      final_state != nullptr, v);
+                                                      final_state != nullptr, variant);
+    if (need == (size_t)-1) return SSM_ERR_DIMS;
     if (!device_buffer || device_buffer_bytes < need || !aligned(device_buffer, 256))
         return SSM_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t es = elem_size(io_dtype);
     const size_t nx = (size_t)batch * dim * (size_t)seqlen * es;
     const size_t nb = (size_t)batch * dstate * (size_t)seqlen * es;
+    const size_t ns = (size_t)batch * dim * dstate * 4;
+    const HostPlan hp = host_plan(batch, dim, seqlen, io_dtype, z != nullptr);
+    size_t wsb = 0;
+    for (const int64_t len : {hp.len, hp.last}) {
+        const size_t w = workspace_for(batch, dim, dstate, len, resolve_variant(batch, dim, dstate, len, io_dtype, variant));
+        wsb = w > wsb ? w : wsb;
+    }
     char *cur = static_cast<char *>(device_buffer);
     auto carve = [&](size_t bytes) { char *r = cur; cur += round256(bytes); return r; };
-    void *ws = carve(workspace_for(batch, dim, dstate, seqlen, v));
-    void *dx = carve(nx), *dd = carve(nx), *dy = carve(nx);
-    void *dz = z ? carve(nx) : nullptr;
-    void *dB = carve(nb), *dC = carve(nb);
+    char *ws = carve(wsb);
+    char *dx = carve(nx), *dd = carve(nx), *dy = carve(nx);
+    char *dz = z ? carve(nx) : nullptr;
+    char *dB = carve(nb), *dC = carve(nb);
     float *dA = reinterpret_cast<float *>(carve((size_t)dim * dstate * 4));
     float *dD = D ? reinterpret_cast<float *>(carve((size_t)dim * 4)) : nullptr;
     float *dbias = dt_bias ? reinterpret_cast<float *>(carve((size_t)dim * 4)) : nullptr;
-    float *dfs = final_state ? reinterpret_cast<float *>(carve((size_t)batch * dim * dstate * 4)) : nullptr;
-    struct Copy { void *dst; const void *src; size_t n; };
-    const Copy in[] = {{dx, x, nx}, {dd, delta, nx}, {dz, z, z ? nx : 0}, {dB, B, nb}, {dC, C, nb},
-                       {dA, A, (size_t)dim * dstate * 4}, {dD, D, D ? (size_t)dim * 4 : 0},
-                       {dbias, dt_bias, dt_bias ? (size_t)dim * 4 : 0}};
-    for (const Copy &c : in)
-        if (c.n && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, st) != cudaSuccess)
-            return SSM_ERR_LAUNCH;
-    rc = ssm_scan_fwd_variant(dx, dd, dA, dB, dC, dD, dz, dbias, delta_softplus, dy, dfs, batch, dim,
-                              dstate, seqlen, io_dtype, ws, round256(workspace_for(batch, dim, dstate, seqlen, v)),
-                              stream, v);
+    float *dstate_buf = reinterpret_cast<float *>(carve(ns));
+
+    HostStreams *hs = host_streams();
+    if (!hs) return SSM_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lk(hs->mu);
+    // Everything already queued on `stream` comes first; the copy streams
+    // join it, and the call returns only after all three are idle.
+    bool fail = cudaEventRecord(hs->start, st) != cudaSuccess ||
+                cudaStreamWaitEvent(hs->in, hs->start, 0) != cudaSuccess ||
+                cudaStreamWaitEvent(hs->out, hs->start, 0) != cudaSuccess;
+    const struct { void *dst; const void *src; size_t n; } small[] = {
+        {dA, A, (size_t)dim * dstate * 4}, {dD, D, D ? (size_t)dim * 4 : 0},
+        {dbias, dt_bias, dt_bias ? (size_t)dim * 4 : 0}};
+    for (const auto &c : small)
+        if (!fail && c.n) fail = cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, hs->in) != cudaSuccess;
+    const size_t rows = (size_t)batch * dim, brows = (size_t)batch * dstate, pitch = (size_t)seqlen * es;
+    if (seqlen == 0 || rows == 0) {
+        // nothing to copy in; the forward still sets final_state (zeros)
+        if (!fail) fail = cudaEventRecord(hs->ready[0], hs->in) != cudaSuccess ||
+                          cudaStreamWaitEvent(st, hs->ready[0], 0) != cudaSuccess;
+        if (!fail) rc = ssm_scan_fwd_variant(dx, dd, dA, dB, dC, dD, dz, dbias, delta_softplus, dy,
+                                             final_state ? dstate_buf : nullptr, batch, dim, dstate, seqlen,
+                                             io_dtype, ws, wsb, stream, variant);
+        if (!fail && rc == SSM_OK && final_state && ns)
+            fail = cudaMemcpyAsync(final_state, dstate_buf, ns, cudaMemcpyDeviceToHost, st) != cudaSuccess;
+    } else {
+        for (int j = 0; j < hp.n && !fail && rc == SSM_OK; ++j) {
+            // chunk j: steps [t0, t0 + len), stored chunk after chunk in the device
+            // buffers, each chunk's rows contiguous
+            const int64_t t0 = (int64_t)j * hp.len;
+            const int64_t len = j + 1 < hp.n ? hp.len : hp.last;
+            const size_t wb = (size_t)len * es, off = (size_t)t0 * es;
+            char *cx = dx + rows * off, *cd = dd + rows * off, *cy = dy + rows * off;
+            char *cz = dz ? dz + rows * off : nullptr;
+            char *cB = dB + brows * off, *cC = dC + brows * off;
+            const struct { char *dst; const void *src; size_t h; } in[] = {
+                {cx, x, rows}, {cd, delta, rows}, {cz, z, z ? rows : 0}, {cB, B, brows}, {cC, C, brows}};
+            for (const auto &c : in)
+                if (!fail && c.h)
+                    fail = cudaMemcpy2DAsync(c.dst, wb, static_cast<const char *>(c.src) + off, pitch, wb, c.h,
+                                             cudaMemcpyHostToDevice, hs->in) != cudaSuccess;
+            if (fail) break;
+            fail = cudaEventRecord(hs->ready[j], hs->in) != cudaSuccess ||
+                   cudaStreamWaitEvent(st, hs->ready[j], 0) != cudaSuccess;
+            if (fail) break;
+            rc = fwd_device(cx, cd, dA, cB, cC, dD, cz, dbias, delta_softplus, j ? dstate_buf : nullptr, cy,
+                            dstate_buf, batch, dim, dstate, len, io_dtype, ws, wsb, stream, variant);
+            if (rc != SSM_OK) break;
+            fail = cudaEventRecord(hs->done[j], st) != cudaSuccess ||
+                   cudaStreamWaitEvent(hs->out, hs->done[j], 0) != cudaSuccess ||
+                   cudaMemcpy2DAsync(static_cast<char *>(y) + off, pitch, cy, wb, wb, rows, cudaMemcpyDeviceToHost,
+                                     hs->out) != cudaSuccess;
+        }
+        if (!fail && rc == SSM_OK && final_state)
+            fail = cudaMemcpyAsync(final_state, dstate_buf, ns, cudaMemcpyDeviceToHost, hs->out) != cudaSuccess;
+    }
+    // Wait for every queued copy before returning, also after a failure: the
+    // copies read and write the caller's host buffers.
+    const bool s1 = cudaStreamSynchronize(hs->in) == cudaSuccess;
+    const bool s2 = cudaStreamSynchronize(st) == cudaSuccess;
+    const bool s3 = cudaStreamSynchronize(hs->out) == cudaSuccess;
     if (rc != SSM_OK) return rc;
-    if (nx && cudaMemcpyAsync(y, dy, nx, cudaMemcpyDeviceToHost, st) != cudaSuccess) return SSM_ERR_LAUNCH;
-    if (dfs && cudaMemcpyAsync(final_state, dfs, (size_t)batch * dim * dstate * 4, cudaMemcpyDeviceToHost,
-                               st) != cudaSuccess)
-        return SSM_ERR_LAUNCH;
-    return cudaStreamSynchronize(st) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    return (!fail && s1 && s2 && s3) ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
 }  // extern "C"

@@ -211,6 +211,33 @@ def test_host_entry_point_matches_device():
     assert_close(fs.numpy().reshape(60, 16), fr, "f32", "host final_state")
 
 
+@pytest.mark.parametrize("batch,dim,L,dtype,gate", [
+    (2, 1024, 4096, "bf16", True),     # three aligned time chunks
+    (2, 1024, 4100, "bf16", True),     # ragged last chunk: rows not 16-byte aligned, element-load path
+    (1, 256, 40000, "f32", False),     # three chunks, each scanned by the two-pass variant
+])
+def test_host_entry_point_time_chunks(batch, dim, L, dtype, gate):
+    """Problems of 16 MiB or more go through the host entry point in time
+    chunks, each starting from the state the previous one ended in.  The
+    result matches the oracle on sampled channels and the single-call device
+    path everywhere within the tolerance."""
+    p = synth.make_problem(batch, dim, 16, L, dtype=dtype, gate=gate, seed=87 + L)
+    pin = lambda a: None if a is None else a.pin_memory()
+    fs = torch.empty(batch, dim, 16).pin_memory()
+    y = ssm.scan_fwd_host(pin(p.x), pin(p.delta), pin(p.A), pin(p.B), pin(p.C), D=pin(p.D), z=pin(p.z),
+                          dt_bias=pin(p.dt_bias), delta_softplus=p.delta_softplus, final_state=fs)
+    nch = batch * dim
+    yh = y.float().numpy().reshape(nch, L)
+    yd, fd = run_gpu(p)
+    assert_close(yh, yd.reshape(nch, L).astype(np.float64), dtype, "host y vs device y")
+    assert_close(fs.numpy().reshape(nch, 16), fd.reshape(nch, 16).astype(np.float64), "f32",
+                 "host final_state vs device final_state")
+    ch = _sample_channels(p, 6, seed=88)
+    yr, fr = run_oracle(p, ch)
+    assert_close(yh[ch], yr, dtype, "host y vs oracle")
+    assert_close(fs.numpy().reshape(nch, 16)[ch], fr, "f32", "host final_state vs oracle")
+
+
 # ----------------------------------------------------- full-size workloads
 def _sample_channels(p, k, seed):
     nch = p.batch * p.dim
