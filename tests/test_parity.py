@@ -211,21 +211,29 @@ def test_host_entry_point_matches_device():
     assert_close(fs.numpy().reshape(60, 16), fr, "f32", "host final_state")
 
 
-@pytest.mark.parametrize("batch,dim,L,dtype,gate", [
-    (2, 1024, 4096, "bf16", True),     # three aligned time chunks
-    (2, 1024, 4100, "bf16", True),     # ragged last chunk: rows not 16-byte aligned, element-load path
-    (1, 256, 40000, "f32", False),     # three chunks, each scanned by the two-pass variant
+@pytest.mark.parametrize("batch,dim,L,dtype,gate,pinned_y", [
+    (2, 1024, 4096, "bf16", True, True),     # three aligned time chunks
+    (2, 1024, 4096, "bf16", True, False),    # the same into a pageable y
+    (2, 1024, 4100, "bf16", True, True),     # ragged last chunk: rows not 16-byte aligned, element-load path
+    (1, 256, 40000, "f32", False, True),     # three chunks, each scanned by the two-pass variant
+    (1, 256, 40000, "f32", False, False),
+    (2, 30, 500, "bf16", True, True),        # one chunk
 ])
-def test_host_entry_point_time_chunks(batch, dim, L, dtype, gate):
+def test_host_entry_point_time_chunks(batch, dim, L, dtype, gate, pinned_y):
     """Problems of 16 MiB or more go through the host entry point in time
-    chunks, each starting from the state the previous one ended in.  The
-    result matches the oracle on sampled channels and the single-call device
-    path everywhere within the tolerance."""
+    chunks, each starting from the state the previous one ended in, into a
+    page-locked or a pageable y.  The result matches the oracle on sampled
+    channels and the single-call device path everywhere within the
+    tolerance."""
     p = synth.make_problem(batch, dim, 16, L, dtype=dtype, gate=gate, seed=87 + L)
     pin = lambda a: None if a is None else a.pin_memory()
     fs = torch.empty(batch, dim, 16).pin_memory()
+    y0 = torch.full_like(p.x, float("nan"))
+    y0 = y0.pin_memory() if pinned_y else y0
+    assert y0.is_pinned() == pinned_y
     y = ssm.scan_fwd_host(pin(p.x), pin(p.delta), pin(p.A), pin(p.B), pin(p.C), D=pin(p.D), z=pin(p.z),
-                          dt_bias=pin(p.dt_bias), delta_softplus=p.delta_softplus, final_state=fs)
+                          dt_bias=pin(p.dt_bias), delta_softplus=p.delta_softplus, y=y0, final_state=fs)
+    assert y is y0
     nch = batch * dim
     yh = y.float().numpy().reshape(nch, L)
     yd, fd = run_gpu(p)
