@@ -79,10 +79,13 @@ typedef enum {
  *            third approach).  Workspace: B and C re-laid out once per call
  *            as float32 rows (batch * seqlen * (2 * padded dstate + 16) * 4
  *            bytes, padded dstate = 8, 16, 32 or 64).
- *  CHUNKED : each warp scans a chunk of 32*k steps: every lane runs k steps
- *            serially, a warp-shuffle Hillis-Steele scan combines the lanes'
- *            (a, b) totals, and the state is carried from chunk to chunk
- *            (sect. 2.1 hybrid, sect. 3.2 warp shuffle).  No workspace.
+ *  CHUNKED : time-parallel.  One warp per channel scans chunks of 32*k
+ *            steps: every lane folds its k steps, a warp-shuffle
+ *            Hillis-Steele scan per state pair combines the lanes' (a, b)
+ *            totals, and the state is carried from chunk to chunk (sect. 2.1
+ *            hybrid, sect. 3.2 warp shuffle).  Workspace: B and C re-laid out
+ *            per chunk, batch * ceil(seqlen / 32k) * ceil(dstate / 2) * 32k
+ *            * 16 bytes (k = 8, or 4 above 32 states).
  *  TWOPASS : the sequence is cut into chunks processed in parallel; pass 1
  *            writes every chunk's total (A_k, B_k), a small scan over the
  *            chunk totals gives each chunk's start state, and pass 2 re-runs

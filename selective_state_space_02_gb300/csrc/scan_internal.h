@@ -32,7 +32,7 @@ struct FwdArgs {
 
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t s);
-cudaError_t launch_chunked(const FwdArgs &a, cudaStream_t s);
+cudaError_t launch_chunked(const FwdArgs &a, void *workspace, cudaStream_t s);
 cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t s);
 
 // States at the start of every segment of seg_len steps (segment 0 starts
@@ -52,6 +52,9 @@ int read_device_status(cudaStream_t st, bool clear, unsigned int *out);
 
 // Workspace bytes of the fused variant (B/C prepared as float32 rows).
 size_t fused_workspace_bytes(int batch, int dim, int dstate, int64_t L);
+
+// Workspace bytes of the chunked variant (B/C prepared per chunk).
+size_t chunked_workspace_bytes(int batch, int dim, int dstate, int64_t L);
 
 // Chunk length and workspace bytes of the two-pass variant.
 int64_t twopass_chunk_len(int batch, int dim, int dstate, int64_t L);

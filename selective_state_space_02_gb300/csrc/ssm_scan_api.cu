@@ -82,6 +82,7 @@ size_t workspace_for(int batch, int dim, int dstate, int64_t seqlen, int variant
     if (batch <= 0 || dim <= 0 || seqlen <= 0) return 0;
     if (variant == SSM_VARIANT_TWOPASS) return ssm::twopass_workspace_bytes(batch, dim, dstate, seqlen);
     if (variant == SSM_VARIANT_FUSED) return ssm::fused_workspace_bytes(batch, dim, dstate, seqlen);
+    if (variant == SSM_VARIANT_CHUNKED) return ssm::chunked_workspace_bytes(batch, dim, dstate, seqlen);
     return 0;
 }
 
@@ -244,7 +245,7 @@ int fwd_device(const void *x, const void *delta, const float *A, const void *B, 
     cudaError_t e;
     switch (v) {
         case SSM_VARIANT_FUSED: e = ssm::launch_fused(a, workspace, st); break;
-        case SSM_VARIANT_CHUNKED: e = ssm::launch_chunked(a, st); break;
+        case SSM_VARIANT_CHUNKED: e = ssm::launch_chunked(a, workspace, st); break;
         case SSM_VARIANT_TWOPASS: e = ssm::launch_twopass(a, workspace, st); break;
         default: return SSM_ERR_VARIANT;
     }

@@ -74,7 +74,10 @@ def _r256(n):
 
 
 def test_workspace_sizes(lib):
-    assert ssm.workspace_size(4, 1536, 16, 2048, variant="chunked") == 0
+    # chunked: B and C per chunk of 32 K steps as float4 per (state pair, step); K = 8, or 4 above 32 states
+    assert ssm.workspace_size(4, 1536, 16, 2048, variant="chunked") == _r256(4 * 8 * 8 * 256 * 16)
+    assert ssm.workspace_size(2, 5120, 64, 8192, variant="chunked") == _r256(2 * 64 * 32 * 128 * 16)
+    assert ssm.workspace_size(1, 8, 5, 100, variant="chunked") == _r256(1 * 1 * 3 * 256 * 16)
     # fused: B and C prepared once as float32 rows [batch * L][2 * padded dstate + 16]
     assert ssm.workspace_size(4, 1536, 16, 2048, variant="fused") == _r256(4 * 2048 * 48 * 4)
     assert ssm.workspace_size(2, 5120, 64, 8192, variant="fused") == _r256(2 * 8192 * 144 * 4)
