@@ -46,8 +46,9 @@ SM_MAX_MHZ = 2070.0            # maximum SM clock
 UPDATES_PER_CLK_SM = 32        # (t,d,n) updates per clock per SM: 128 FP32 lanes / 4 ops, 32 ex2/clk
 HBM_FALLBACK_GBS = 6800.0
 # kernels this library launches per step: fused = B/C re-layout + scan;
-# two-pass = re-layout + pass 1 + segment carry + pass 2; chunked = scan
-KERNELS_PER_STEP = {"fused": 2, "chunked": 1, "twopass": 4}
+# two-pass = re-layout + pass 1 + segment carry + pass 2; chunked = B/C chunk
+# re-layout + scan
+KERNELS_PER_STEP = {"fused": 2, "chunked": 2, "twopass": 4}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.json")
 _FUSED_SOURCES = ["selective_state_space_02_gb300/csrc/scan_fused_impl.cuh",
                   "selective_state_space_02_gb300/csrc/scan_fused_dispatch.cuh",
@@ -58,7 +59,8 @@ KERNEL_SOURCES = {
     "fused": _FUSED_SOURCES,
     "twopass": _FUSED_SOURCES,
     "chunked": ["selective_state_space_02_gb300/csrc/scan_chunked.cu",
-                "selective_state_space_02_gb300/csrc/scan_device.cuh"],
+                "selective_state_space_02_gb300/csrc/scan_device.cuh",
+                "selective_state_space_02_gb300/csrc/scan_tma.cuh"],
 }
 
 
@@ -342,7 +344,7 @@ def run_ours(args):
         "unit": "Tupdate/s",
         "frac": round(alu_achieved / alu_peak, 4),
         "traffic": traffic,
-        "kernel": f"{variant} scan step (B/C re-layout, ~3% of it, plus the scan kernel)" if variant != "chunked" else "chunked scan",
+        "kernel": f"{variant} scan step (B/C re-layout, ~3% of it, plus the scan kernel)" if variant != "chunked" else "chunked scan step (B/C chunk re-layout plus the scan kernel)",
         "peak_basis": f"{SMS} SMs x {SM_MAX_MHZ:.0f} MHz x {UPDATES_PER_CLK_SM} (t,d,n) updates/clk/SM "
                       "(1 ex2 + 4 FP32 ops per update; 32 ex2 and 128 FP32 lanes per clk per SM)",
         "hbm": {"achieved": round(hbm_gbs, 1), "peak": hbm_peak, "unit": "GB/s",

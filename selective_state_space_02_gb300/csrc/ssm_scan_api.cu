@@ -183,12 +183,15 @@ const char *ssm_scan_status_string(int status) {
 int ssm_scan_select_variant(int batch, int dim, int dstate, int64_t seqlen, int io_dtype) {
     if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!valid_sizes(batch, dim, dstate, seqlen)) return SSM_ERR_DIMS;
-    // Channel-parallel walking fills the GPU when there are enough channels
-    // (or the sequence is short); otherwise the sequence is cut into
-    // segments combined by the two-pass chunk carry.  The warp-shuffle
-    // CHUNKED variant is available on request.
+    // Channel-parallel walking wins once there are enough channels to keep
+    // the GPU busy.  With fewer, short sequences go to the time-parallel
+    // CHUNKED variant and longer ones are cut into segments combined by the
+    // two-pass chunk carry (timed on GB300 over 64-4096 channels and 256-8192
+    // steps, bf16 and f32).
     const int64_t nchan = (int64_t)batch * dim;
-    if (nchan >= 4096 || seqlen <= 2048) return SSM_VARIANT_FUSED;
+    if (nchan >= 4096) return SSM_VARIANT_FUSED;
+    if (seqlen <= 1024) return SSM_VARIANT_CHUNKED;
+    if (seqlen <= 2048 && nchan > 1024) return SSM_VARIANT_FUSED;
     return SSM_VARIANT_TWOPASS;
 }
 

@@ -64,6 +64,9 @@ def test_variant_selection_host_only(lib):
     assert ssm.select_variant(2, 5120, 64, 8192) == "fused"
     assert ssm.select_variant(1, 768, 16, 131072) == "twopass"
     assert ssm.select_variant(1, 64, 16, 1 << 20) == "twopass"
+    assert ssm.select_variant(1, 64, 16, 256) == "chunked"
+    assert ssm.select_variant(2, 1024, 16, 2048) == "fused"
+    assert ssm.select_variant(1, 512, 16, 2048) == "twopass"
     assert lib.ssm_scan_select_variant(1, 1, 0, 10, 0) == ERR_DIMS
     assert lib.ssm_scan_select_variant(1, 1, 65, 10, 0) == ERR_DIMS
     assert lib.ssm_scan_select_variant(1, 1, 16, 10, 3) == ERR_DTYPE
