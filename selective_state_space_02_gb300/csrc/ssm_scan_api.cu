@@ -97,24 +97,43 @@ size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 // problems: fewer leave the scan and the copy back exposed, more let the copy
 // back slow the copy in for longer and add per-chunk overhead.  Problems of
 // 48 MiB or more (x, delta, z and y) run in three chunks, from 16 MiB in two,
-// smaller ones in one; every chunk but the last is a whole number of 64-step
-// tiles (16-byte aligned rows in either dtype).
+// smaller ones in one; chunk boundaries fall on whole 64-step tiles (16-byte
+// aligned rows in either dtype), so only the last chunk can be ragged.
 constexpr int kMaxHostChunks = 3;
 
 struct HostPlan {
-    int64_t len;    // steps per chunk
-    int64_t last;   // steps of the last chunk
-    int n;          // number of chunks
+    int64_t start[kMaxHostChunks + 1];   // chunk j covers steps [start[j], start[j + 1])
+    int n;                               // number of chunks
+    int64_t len(int j) const { return start[j + 1] - start[j]; }
 };
+
+// Chunk shares of the sequence, largest first: the last chunk's scan and copy
+// back are the exposed tail of the pipeline.  0.40 / 0.35 / 0.25 measured
+// 1-5% faster than equal thirds on the 100 MB - 1.2 GB problems.
+constexpr double kShare2[2] = {0.55, 0.45};
+constexpr double kShare3[3] = {0.40, 0.35, 0.25};
 
 HostPlan host_plan(int batch, int dim, int64_t seqlen, int io_dtype, bool has_z) {
     const size_t bytes = (size_t)batch * dim * (size_t)seqlen * elem_size(io_dtype) * (has_z ? 4 : 3);
-    const int64_t k = bytes >= ((size_t)48 << 20) ? 3 : bytes >= ((size_t)16 << 20) ? 2 : 1;
-    int64_t len = k > 1 ? (seqlen + k - 1) / k : seqlen;
-    len = (len + 63) / 64 * 64;
-    if (len >= seqlen) return HostPlan{seqlen, seqlen, 1};
-    const int n = (int)((seqlen + len - 1) / len);
-    return HostPlan{len, seqlen - (int64_t)(n - 1) * len, n};
+    const int k = bytes >= ((size_t)48 << 20) ? 3 : bytes >= ((size_t)16 << 20) ? 2 : 1;
+    const double *share = k == 3 ? kShare3 : kShare2;
+    HostPlan hp{};
+    hp.start[0] = 0;
+    hp.n = 0;
+    double acc = 0.0;
+    for (int j = 0; j < k; ++j) {
+        int64_t end = seqlen;
+        if (j + 1 < k) {
+            acc += share[j];
+            end = ((int64_t)(acc * (double)seqlen) + 63) / 64 * 64;   // whole 64-step tiles
+        }
+        if (end <= hp.start[hp.n]) continue;
+        if (end > seqlen) end = seqlen;
+        hp.start[++hp.n] = end;
+        if (end == seqlen) break;
+    }
+    if (hp.n == 0) { hp.start[1] = seqlen; hp.n = 1; }
+    return hp;
 }
 
 // Copy streams and events of one device for the host-buffer entry point,
@@ -301,7 +320,8 @@ size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seq
     if (resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant) < 0) return (size_t)-1;
     const HostPlan hp = host_plan(batch, dim, seqlen, io_dtype, has_z != 0);
     size_t ws = 0;
-    for (const int64_t len : {hp.len, hp.last}) {
+    for (int j = 0; j < hp.n; ++j) {
+        const int64_t len = hp.len(j);
         const int v = resolve_variant(batch, dim, dstate, len, io_dtype, variant);
         if (v < 0) return (size_t)-1;
         const size_t w = workspace_for(batch, dim, dstate, len, v);
@@ -342,7 +362,8 @@ int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const vo
     const size_t ns = (size_t)batch * dim * dstate * 4;
     const HostPlan hp = host_plan(batch, dim, seqlen, io_dtype, z != nullptr);
     size_t wsb = 0;
-    for (const int64_t len : {hp.len, hp.last}) {
+    for (int j = 0; j < hp.n; ++j) {
+        const int64_t len = hp.len(j);
         const size_t w = workspace_for(batch, dim, dstate, len, resolve_variant(batch, dim, dstate, len, io_dtype, variant));
         wsb = w > wsb ? w : wsb;
     }
@@ -384,8 +405,8 @@ int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const vo
         for (int j = 0; j < hp.n && !fail && rc == SSM_OK; ++j) {
             // chunk j: steps [t0, t0 + len), stored chunk after chunk in the device
             // buffers, each chunk's rows contiguous
-            const int64_t t0 = (int64_t)j * hp.len;
-            const int64_t len = j + 1 < hp.n ? hp.len : hp.last;
+            const int64_t t0 = hp.start[j];
+            const int64_t len = hp.len(j);
             const size_t wb = (size_t)len * es, off = (size_t)t0 * es;
             char *cx = dx + rows * off, *cd = dd + rows * off, *cy = dy + rows * off;
             char *cz = dz ? dz + rows * off : nullptr;
