@@ -434,8 +434,9 @@ __global__ void adj_carry_kernel(const float *__restrict__ A, const float *__res
 }
 
 // Segments of chunks: one CTA walks one segment.  Problems whose channels
-// fill a wave (3 CTAs per SM fit at once) keep one segment -- there the walk
-// is bound by the SMs' throughput and the totals pass would be pure cost.
+// fill at least half a wave (3 CTAs per SM fit at once) keep one segment --
+// the totals pass costs more than the extra parallelism gives there (the
+// mid-size shape's 384 CTAs: 0.87 ms unsegmented, 0.99 ms in 5 segments).
 // Fewer channels get segments enough for about four waves (measured best on
 // the long-sequence shape: shorter serial walks, and the totals pass walks
 // shorter segments too); the adjoint entering each segment then comes from the
@@ -444,7 +445,11 @@ constexpr int64_t kWaveCtas = 152 * 3;
 constexpr int64_t kTargetCtas = 4 * kWaveCtas;
 
 int padded_np(int dstate) { return dstate <= 8 ? 8 : dstate <= 16 ? 16 : dstate <= 32 ? 32 : 64; }
-int cta_channels(int np) { return kWarps * (32 / (np < 32 ? np : 32)); }
+// Channels per CTA of the reverse walk for a padded state count (the
+// kernel's own Shape, so the segment plan and the launch agree).
+int cta_channels(int np) {
+    return np == 8 ? Shape<8>::CPC : np == 16 ? Shape<16>::CPC : np == 32 ? Shape<32>::CPC : Shape<64>::CPC;
+}
 
 struct Plan {
     int seg_chunks;   // chunks per segment
@@ -455,7 +460,7 @@ Plan plan_for(int batch, int dim, int dstate, int64_t L) {
     const int nchunk = (int)((L + kChunk - 1) / kChunk);
     const int cpc = cta_channels(padded_np(dstate));
     const int64_t ncta = (int64_t)batch * ((dim + cpc - 1) / cpc);
-    if (nchunk <= 1 || ncta >= kWaveCtas) return Plan{nchunk > 0 ? nchunk : 1, 1};
+    if (nchunk <= 1 || 2 * ncta >= kWaveCtas) return Plan{nchunk > 0 ? nchunk : 1, 1};
     const int64_t want = (kTargetCtas + ncta - 1) / ncta;
     const int seg = (int)((nchunk + want - 1) / want);
     return Plan{seg, (nchunk + seg - 1) / seg};
