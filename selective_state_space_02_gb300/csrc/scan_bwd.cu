@@ -81,7 +81,12 @@ struct Shape {
     // shared memory layout, in floats
     static constexpr int IR = kChunk + 1;           // padded per-channel row of the step inputs
     static constexpr int BR = NP + 1;               // padded B/C row (float2)
-    static constexpr int TR = CPC * NP + 1;         // padded dB/dC term block of one step (float2)
+    // dB/dC term rows: channel stride CS and step stride TR (float2) chosen so
+    // that a warp's term stores (CPW channels x LPC lanes) and the reduction's
+    // reads (8 steps x 4 states per warp) each take the minimum two wavefronts
+    static constexpr int CS = NP == 16 ? NP + 8 : NP;
+    static constexpr int TR = CPC * CS + 4;
+    static_assert(TR % 16 == 4, "term row stride");
     static constexpr int o_in = 0;                           // float4 [CPC][IR]: Delta, u, dq, x
     static constexpr int o_sz = o_in + 4 * IR * CPC;         // float2 [CPC][IR]: softplus'(v), dy silu'(z)
     static constexpr int o_bc = o_sz + 2 * IR * CPC;         // float2 [kChunk][BR]: B, C
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
                         du = fmaf(lam[s], BC.x, du);
                         ds = fmaf(daa, Av[s], ds);
                         pp = fmaf(BC.y, h[s][jl + 1], pp);
-                        tb[jj * TR + c * NP + n] = make_float2(lam[s] * q.y, q.z * h[s][jl + 1]);
+                        tb[jj * TR + c * Sh::CS + n] = make_float2(lam[s] * q.y, q.z * h[s][jl + 1]);
                         lam[s] *= a;
                     }
                     ta[(jj * CPC + c) * LPC + li] = make_float4(du, ds, pp, 0.0f);
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
                         float db = 0.0f, dc = 0.0f;
 #pragma unroll
                         for (int cc = 0; cc < CPC; ++cc) {
-                            const float2 t = tb[jj * TR + cc * NP + n];
+                            const float2 t = tb[jj * TR + cc * Sh::CS + n];
                             db += t.x;
                             dc += t.y;
                         }
