@@ -246,6 +246,20 @@ def test_host_entry_point_time_chunks(batch, dim, L, dtype, gate, pinned_y):
     assert_close(fs.numpy().reshape(nch, 16)[ch], fr, "f32", "host final_state vs oracle")
 
 
+@pytest.mark.parametrize("variant", ["fused", "chunked", "twopass"])
+def test_host_entry_point_explicit_variants(variant):
+    """Every variant through the time-chunked host path (three chunks), with
+    pageable inputs and output and the optional operands absent."""
+    p = synth.make_problem(2, 1024, 16, 4096, dtype="bf16", gate=False, use_D=False, use_dt_bias=False, seed=95)
+    y = ssm.scan_fwd_host(p.x, p.delta, p.A, p.B, p.C, delta_softplus=p.delta_softplus, variant=variant)
+    assert not y.is_pinned()
+    yd, _ = run_gpu(p, variant=variant, final_state=False)
+    assert_close(y.float().numpy(), yd.astype(np.float64), "bf16", f"host y vs device y [{variant}]")
+    ch = _sample_channels(p, 4, seed=96)
+    yr, _ = run_oracle(p, ch)
+    assert_close(y.float().numpy().reshape(-1, p.seqlen)[ch], yr, "bf16", f"host y vs oracle [{variant}]")
+
+
 # ----------------------------------------------------- full-size workloads
 def _sample_channels(p, k, seed):
     nch = p.batch * p.dim
