@@ -281,9 +281,6 @@ size_t chunk_states_workspace_bytes(int batch, int dim, int dstate, int64_t L, i
 }
 
 cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspace, cudaStream_t st) {
-    // The first two steps of the two-pass forward with segments of seg_len
-    // steps: per-segment totals from the zero state, then the carry scan over
-    // the segments seeded with the start state.
     const int nseg = (int)((a.L + seg_len - 1) / seg_len);
     const int64_t nchan = (int64_t)a.batch * a.dim;
     size_t hbytes = (size_t)nseg * nchan * a.dstate * sizeof(float);
@@ -292,8 +289,25 @@ cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspac
     sbytes = (sbytes + 255) / 256 * 256;
     char *ws = static_cast<char *>(workspace);
     fused::SegArgs sg{seg_len, nseg, reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes),
-                      reinterpret_cast<const float *>(ws + hbytes + sbytes)};
-    const int cfg = twopass_cfg(padded_states(a.dstate));
+                      reinterpret_cast<const float *>(ws + hbytes + sbytes), seg_len};
+    // With channels for at least one consumer warp per SM sub-partition, one
+    // pass of the whole-sequence kernel from the start state writes the state
+    // at every segment start as it goes.
+    const int np = padded_states(a.dstate);
+    const int wcfg = choose_cfg(nchan, np, 1);
+    bool whole = nchan / warp_channels(np, wcfg, true) >= (int64_t)kSMs * 4 && seg_len % fused::tile_steps(np) == 0;
+#ifdef SSM_TUNE
+    if (const char *e = std::getenv("SSM_CKPT")) whole = whole && std::atoi(e) != 0;
+#endif
+    if (whole) {
+        sg.seg_len = a.L;
+        sg.nseg = 1;
+        return launch_mode(a, sg, fused::kStates, wcfg, true, st);
+    }
+    // Otherwise the first two steps of the two-pass forward with segments of
+    // seg_len steps: per-segment totals from the zero state, then the carry
+    // scan over the segments seeded with the start state.
+    const int cfg = twopass_cfg(np);
     cudaError_t e = cudaSuccess;
     if (nseg > 1) {
         fused::SegArgs s1 = sg;

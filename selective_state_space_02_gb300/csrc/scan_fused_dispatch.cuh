@@ -22,6 +22,8 @@ cudaError_t by_mode(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, u
                         : launch_one<T, NP, S, NW, false, kWhole, TMA>(a, sg, maps, status, st);
         case kTotals:
             return launch_one<T, NP, S, NW, false, kTotals, TMA>(a, sg, maps, status, st);
+        case kStates:
+            return launch_one<T, NP, S, NW, false, kStates, TMA>(a, sg, maps, status, st);
         default:
             return gate ? launch_one<T, NP, S, NW, true, kSeeded, TMA>(a, sg, maps, status, st)
                         : launch_one<T, NP, S, NW, false, kSeeded, TMA>(a, sg, maps, status, st);

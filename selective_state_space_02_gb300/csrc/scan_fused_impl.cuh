@@ -66,7 +66,10 @@ __host__ __device__ constexpr int blk_steps(int S) { return S <= 4 ? 32 : 16; }
 // 2, the finer grain.
 __host__ __device__ constexpr int consumer_warps(int S) { return S >= 16 ? 3 : 2; }
 
-enum Mode { kWhole = 0, kTotals = 1, kSeeded = 2 };
+// kWhole: y (and the final state) over whole sequences; kTotals: per-segment
+// totals of the two-pass variant, no y; kSeeded: y from each segment's start
+// state; kStates: no y, the state at the start of every ck_len-step chunk.
+enum Mode { kWhole = 0, kTotals = 1, kSeeded = 2, kStates = 3 };
 
 struct SegArgs {
     int64_t seg_len;   // steps per segment (the last one may be shorter)
@@ -74,6 +77,7 @@ struct SegArgs {
     float *ws_h;       // [nseg][batch*dim][dstate]: B_k after pass 1, h_init after the small scan
     float *ws_s;       // [nseg][batch*dim]: sum of Delta over the segment
     const float *bc;   // prepared B/C rows [batch*L][bc_row(NP, S)]
+    int64_t ck_len;    // kStates: steps per chunk (whole tiles); ws_h is then [nchunk][batch*dim][dstate]
 };
 
 // Floats per prepared B/C row: NS groups of S B values and S C values.  A
@@ -100,7 +104,7 @@ struct Layout {
     static constexpr int KB = blk_steps(S);      // steps per block
     static constexpr int E = KB / NS;            // steps each lane owns per block
     static constexpr int TC = tile_steps(NP);
-    static constexpr bool kY = MODE != kTotals;
+    static constexpr bool kY = MODE == kWhole || MODE == kSeeded;
     static constexpr bool kZ = GATE && kY;
     static constexpr size_t row_bytes = (size_t)DT * TC * sizeof(T);
     static constexpr int BCW = bc_row(NP, S);    // floats per prepared B/C row
@@ -407,7 +411,7 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
             const bool ok = dok && n < N;
             v[k] = ok ? __ldg(p.A + (int64_t)d * N + n) * kLog2e : 0.0f;
             hv[k] = (MODE == kSeeded && ok)               ? sg.ws_h[((int64_t)seg * nchan + chan0 + d) * N + n]
-                    : (MODE == kWhole && ok && p.h0)     ? p.h0[(chan0 + d) * N + n]
+                    : (MODE != kSeeded && MODE != kTotals && ok && p.h0) ? p.h0[(chan0 + d) * N + n]
                                                          : 0.0f;
         }
         a2[q] = make_float2(v[0], v[1]);
@@ -428,6 +432,18 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
         const int tvalid = (int)((te - t0) < TC ? (te - t0) : TC);
         const bool ok = wait_parity(&full[st], (uint32_t)((tile / kNST) & 1), status);
         if (!__all_sync(FULL, ok && *abort_flag == 0)) { aborted = true; break; }
+        if constexpr (MODE == kStates) {
+            // the state at the start of every ck_len-step chunk
+            if (dok && t0 % sg.ck_len == 0) {
+                float *dst = sg.ws_h + ((t0 / sg.ck_len) * nchan + chan0 + d) * N;
+#pragma unroll
+                for (int q = 0; q < S / 2; ++q) {
+                    const int n = g * S + 2 * q;
+                    if (n < N) dst[n] = h2[q].x;
+                    if (n + 1 < N) dst[n + 1] = h2[q].y;
+                }
+            }
+        }
 
 #pragma unroll 1
         for (int blk = 0; blk < TC / KB; ++blk) {

@@ -37,8 +37,10 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t s);
 
 // States at the start of every segment of seg_len steps (segment 0 starts
 // from a.h0, or zero), as [nseg][batch*dim][dstate] float32 at the start of
-// `workspace`, computed by the two-pass forward's totals pass and carry scan.
-// The workspace also holds that pass's segment sums and prepared B/C rows.
+// `workspace`.  With channels for one consumer warp per SM sub-partition one
+// whole-sequence pass of the fused kernel writes them as it goes; otherwise
+// the two-pass forward's totals pass and carry scan compute them.  The
+// workspace also holds that pass's segment sums and prepared B/C rows.
 size_t chunk_states_workspace_bytes(int batch, int dim, int dstate, int64_t L, int64_t seg_len);
 cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspace, cudaStream_t st);
 

@@ -80,6 +80,11 @@ def _compare(g, ref, dtype):
     ((2, 7, 64, 45), "bf16", True),       # N = 64: two states per lane
     ((3, 20, 32, 33), "bf16", False),     # N = 32, one step past a chunk
     ((1, 40, 8, 129), "f32", True),       # N = 8: 16 channels per CTA
+    # one consumer warp per SM sub-partition or more: the chunk-start states come from one
+    # whole-sequence forward pass that stores them, not from the totals pass and carry scan
+    ((1, 4880, 16, 100), "f32", True),    # TMA rows, ragged last chunk
+    ((2, 2440, 13, 70), "bf16", False),   # rows not 16-byte aligned (element loads), padded states
+    ((1, 5120, 64, 40), "bf16", True),    # 64 states: 16-step tiles, a state every other tile
 ])
 def test_backward_matches_oracle(shape, dtype, gate):
     p = synth.make_problem(*shape, dtype=dtype, gate=gate, seed=400 + shape[2] + shape[3], A_mode="random")
@@ -92,6 +97,15 @@ def test_backward_with_start_state_and_final_state_gradient():
     h0 = synth.make_state(2, 24, 16, seed=421)
     dfinal = synth.make_state(2, 24, 16, seed=422)
     g, ref = _run(p, _dy(p, 8), h0=h0, dfinal=dfinal)
+    _compare(g, ref, "f32")
+
+
+def test_backward_whole_pass_states_with_start_state():
+    """Chunk-start states from the whole-sequence pass, seeded with a start state."""
+    p = synth.make_problem(1, 4880, 16, 72, dtype="f32", gate=True, seed=429, A_mode="random")
+    h0 = synth.make_state(1, 4880, 16, seed=430)
+    dfinal = synth.make_state(1, 4880, 16, seed=431)
+    g, ref = _run(p, _dy(p, 11), h0=h0, dfinal=dfinal)
     _compare(g, ref, "f32")
 
 
