@@ -657,14 +657,15 @@ def run_bwd(args):
     hbm_peak, peak_kind = measured_peaks()
     kern_s = statistics.mean(per) / 1e3
     mb = bwd_min_bytes(p)
+    bwd_kernels = ssm._native.load().ssm_scan_bwd_kernel_count(p.batch, p.dim, p.dstate, p.seqlen)
     updates = elems * p.dstate
     alu_peak = alu_peak_updates_per_s()
     roofline = {"bound": "alu", "achieved": round(updates / kern_s / 1e12, 4), "peak": round(alu_peak / 1e12, 4),
                 "unit": "Tupdate/s", "frac": round(updates / kern_s / alu_peak, 4), "traffic": None,
-                "kernel": "backward (B/C re-layout, chunk totals, carry scan, reverse walk)",
+                "kernel": "backward (B/C re-layout, chunk-start states, reverse walk)",
                 "peak_basis": f"{SMS} SMs x {SM_MAX_MHZ:.0f} MHz x {UPDATES_PER_CLK_SM} (t,d,n) updates/clk/SM, "
-                              "one ex2 per update (the backward evaluates three: the totals pass, the chunk "
-                              "recomputation and the adjoint)",
+                              "one ex2 per update (the backward evaluates three: the chunk-start states pass, "
+                              "the chunk recomputation and the adjoint)",
                 "hbm": {"achieved": round(mb / kern_s / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
                         "frac": round(mb / kern_s / 1e9 / hbm_peak, 4),
                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
@@ -709,7 +710,7 @@ def run_bwd(args):
                    "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
         "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
-        "gpu_launches": args.steps * 4,   # B/C re-layout, chunk totals, carry scan, reverse walk
+        "gpu_launches": args.steps * bwd_kernels,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -52,6 +52,14 @@ extern "C" {
  * sums and B/C rows prepared as float32); (size_t)-1 for invalid sizes. */
 size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype);
 
+/* Kernels one ssm_scan_bwd call with these sizes launches on the GPU: the
+ * B/C re-layout and the chunk-start states (one whole-sequence pass of the
+ * fused forward where the channels give at least one consumer warp per SM
+ * sub-partition, else a totals pass and a carry scan over the chunks), the
+ * reverse walk, and for walks split into segments the adjoint totals and
+ * their carry.  0 for an empty problem, -1 for invalid sizes.  Host only. */
+int ssm_scan_bwd_kernel_count(int batch, int dim, int dstate, int64_t seqlen);
+
 /*
  *   x, delta, A, B, C, D, z, dt_bias, delta_softplus, initial_state
  *                  the forward's inputs (as ssm_scan_fwd_from_state; D, z,

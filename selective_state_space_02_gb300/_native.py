@@ -44,6 +44,7 @@ SIGNATURES = {
     # x, weight, bias, state_in, y, state_out, silu, batch, dim, seqlen, width, dtype, stream
     "ssm_conv1d_fwd": (_i, [_vp] * 6 + [_i, _i, _i, _i64, _i, _i, _vp]),
     "ssm_scan_bwd_workspace_size": (_sz, [_i, _i, _i, _i64, _i]),
+    "ssm_scan_bwd_kernel_count": (_i, [_i, _i, _i, _i64]),
     # x, delta, A, B, C, D, z, dt_bias, softplus, h0, dy, dfinal, dx, ddelta, dA, dB, dC, dD, dz, ddt_bias,
     # dh0, batch, dim, dstate, seqlen, dtype, workspace, bytes, stream
     "ssm_scan_bwd": (_i, [_vp] * 8 + [_i] + [_vp] * 12 + [_i, _i, _i, _i64, _i, _vp, _sz, _vp]),

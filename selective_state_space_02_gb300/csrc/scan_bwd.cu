@@ -146,6 +146,19 @@ __device__ __forceinline__ void load_raw(const BwdArgs &p, int b, int d0, int k,
     }
 }
 
+// The start state of chunk k for the lane's states (zero outside the problem).
+template <int NP>
+__device__ __forceinline__ void load_start(const BwdArgs &p, int k, int64_t chn, int li, bool dok,
+                                           float (&h)[Shape<NP>::S2]) {
+    constexpr int LPC = Shape<NP>::LPC;
+    const int64_t nchan = (int64_t)p.batch * p.dim;
+#pragma unroll
+    for (int s = 0; s < Shape<NP>::S2; ++s) {
+        const int n = li + LPC * s;
+        h[s] = (dok && n < p.N) ? p.ws_h[((int64_t)k * nchan + chn) * p.N + n] : 0.0f;
+    }
+}
+
 template <typename T, int NP>
 // Three CTAs per SM (at most 168 registers): the walk is latency-bound, and the
 // extra CTA outweighs the few spilled bytes (mid 1.03 -> 0.87 ms, wide 29.4 -> 23.2 ms).
@@ -195,7 +208,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
     const int k_lo = blockIdx.z * p.seg_chunks;
     const int k_hi = k_lo + p.seg_chunks < nchunk ? k_lo + p.seg_chunks : nchunk;
     Raw<NP> raw;
-    if (k_hi > k_lo) load_raw<T, NP>(p, b, d0, k_hi - 1, raw);
+    float hnext[S2];                                    // the next chunk's start state, in flight like raw
+    if (k_hi > k_lo) {
+        load_raw<T, NP>(p, b, d0, k_hi - 1, raw);
+        load_start<NP>(p, k_hi - 1, chn, li, dok, hnext);
+    }
     for (int k = k_hi - 1; k >= k_lo; --k) {
         const int64_t t0 = (int64_t)k * kChunk;
         const int jn = (L - t0) < kChunk ? (int)(L - t0) : kChunk;
@@ -225,12 +242,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
         }
         float hst[S2];                                      // the chunk's start state
 #pragma unroll
-        for (int s = 0; s < S2; ++s) {
-            const int n = li + LPC * s;
-            hst[s] = (dok && n < N) ? p.ws_h[((int64_t)k * nchan + chn) * N + n] : 0.0f;
-        }
+        for (int s = 0; s < S2; ++s) hst[s] = hnext[s];
         __syncthreads();
-        if (k > k_lo) load_raw<T, NP>(p, b, d0, k - 1, raw);   // next chunk's inputs, in flight meanwhile
+        if (k > k_lo) {                                     // next chunk's inputs, in flight meanwhile
+            load_raw<T, NP>(p, b, d0, k - 1, raw);
+            load_start<NP>(p, k - 1, chn, li, dok, hnext);
+        }
         // the chunk in sub-chunks of SC steps, last first: SC + 1 states per
         // state fit in registers; a sub-chunk's start state is advanced from
         // the chunk's start again
@@ -537,6 +554,13 @@ extern "C" size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, in
     const ssm::Plan pl = ssm::plan_for(batch, dim, dstate, seqlen);
     return ssm::r256(ssm::chunk_states_workspace_bytes(batch, dim, dstate, seqlen, ssm::kChunk)) +
            ssm::seg_bytes(pl, (int64_t)batch * dim, dstate);
+}
+
+extern "C" int ssm_scan_bwd_kernel_count(int batch, int dim, int dstate, int64_t seqlen) {
+    if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64 || seqlen < 0) return -1;
+    if (batch == 0 || dim == 0 || seqlen == 0) return 0;
+    const ssm::Plan pl = ssm::plan_for(batch, dim, dstate, seqlen);
+    return ssm::chunk_start_states_kernels(batch, dim, dstate, seqlen, ssm::kChunk) + (pl.nseg > 1 ? 3 : 1);
 }
 
 extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, const void *B, const void *C,

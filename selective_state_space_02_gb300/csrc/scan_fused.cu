@@ -280,6 +280,29 @@ size_t chunk_states_workspace_bytes(int batch, int dim, int dstate, int64_t L, i
     return (h + 255) / 256 * 256 + (s + 255) / 256 * 256 + bc_bytes(batch, dstate, L);
 }
 
+namespace {
+
+// Whether chunk_start_states takes the one-pass route: channels for at least
+// one consumer warp per SM sub-partition, segments of whole tiles.
+bool states_in_one_pass(int batch, int dim, int dstate, int64_t seg_len) {
+    const int64_t nchan = (int64_t)batch * dim;
+    const int np = padded_states(dstate);
+    const int cfg = choose_cfg(nchan, np, 1);
+    bool one = nchan / warp_channels(np, cfg, true) >= (int64_t)kSMs * 4 && seg_len % fused::tile_steps(np) == 0;
+#ifdef SSM_TUNE
+    if (const char *e = std::getenv("SSM_CKPT")) one = one && std::atoi(e) != 0;
+#endif
+    return one;
+}
+
+}  // namespace
+
+int chunk_start_states_kernels(int batch, int dim, int dstate, int64_t L, int64_t seg_len) {
+    if (states_in_one_pass(batch, dim, dstate, seg_len)) return 2;   // B/C re-layout, the pass
+    const int64_t nseg = (L + seg_len - 1) / seg_len;
+    return nseg > 1 ? 3 : 1;                                        // (re-layout, totals,) carry scan
+}
+
 cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspace, cudaStream_t st) {
     const int nseg = (int)((a.L + seg_len - 1) / seg_len);
     const int64_t nchan = (int64_t)a.batch * a.dim;
@@ -295,11 +318,7 @@ cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspac
     // at every segment start as it goes.
     const int np = padded_states(a.dstate);
     const int wcfg = choose_cfg(nchan, np, 1);
-    bool whole = nchan / warp_channels(np, wcfg, true) >= (int64_t)kSMs * 4 && seg_len % fused::tile_steps(np) == 0;
-#ifdef SSM_TUNE
-    if (const char *e = std::getenv("SSM_CKPT")) whole = whole && std::atoi(e) != 0;
-#endif
-    if (whole) {
+    if (states_in_one_pass(a.batch, a.dim, a.dstate, seg_len)) {
         sg.seg_len = a.L;
         sg.nseg = 1;
         return launch_mode(a, sg, fused::kStates, wcfg, true, st);

@@ -43,6 +43,8 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t s);
 // workspace also holds that pass's segment sums and prepared B/C rows.
 size_t chunk_states_workspace_bytes(int batch, int dim, int dstate, int64_t L, int64_t seg_len);
 cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspace, cudaStream_t st);
+// Kernels chunk_start_states launches for these sizes.
+int chunk_start_states_kernels(int batch, int dim, int dstate, int64_t L, int64_t seg_len);
 
 // Device address of the status word of the bounded waits on the current
 // device (nullptr if the lookup fails); kernels OR bit 0 into it.

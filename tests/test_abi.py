@@ -250,3 +250,18 @@ def test_conv_validation(lib):
     assert _conv(lib, x=16 * 2 + 1, dtype=1) == ERR_ALIGN
     assert _conv(lib, y=16 * 2) == ERR_ALIAS                         # y over x
     assert _conv(lib, sin=16 * 100, sout=16 * 100 + 4) == ERR_ALIAS   # state out over state in
+
+
+def test_backward_kernel_count(lib):
+    f = lib.ssm_scan_bwd_kernel_count
+    # B/C re-layout + one whole-sequence pass storing the chunk-start states, one reverse walk
+    assert f(4, 1536, 16, 2048) == 3
+    assert f(8, 2048, 16, 4096) == 3
+    assert f(2, 5120, 64, 8192) == 3
+    # 768 channels: re-layout, chunk totals and carry scan, then a walk split into segments
+    # (adjoint totals, their carry, the walk)
+    assert f(1, 768, 16, 131072) == 6
+    # one chunk: the carry scan alone gives its start state, one walk
+    assert f(1, 8, 16, 20) == 2
+    assert f(0, 8, 16, 20) == 0 and f(1, 8, 16, 0) == 0
+    assert f(1, 8, 65, 20) == -1 and f(-1, 8, 16, 20) == -1
