@@ -1,5 +1,5 @@
-// Channel-parallel, time-serial forward selective scan (FUSED variant, and
-// both passes of the TWOPASS variant).
+// Channel-parallel, time-serial forward selective scan (FUSED variant, both
+// passes of the TWOPASS variant, and the backward's chunk-start states).
 //
 // "Mamba hardware-aware parallel associative scan" (pwwt.cn/news/6375169):
 //   sect. 2.2, third approach -- parallelism over channels; a thread owns part
