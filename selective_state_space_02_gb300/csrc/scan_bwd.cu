@@ -94,7 +94,8 @@ struct Shape {
     static constexpr int o_bc = o_sz + 2 * IR * CPC;         // float2 [kChunk][BR]: B, C
     static constexpr int o_ta = o_bc + 2 * kChunk * BR;      // float4 [F][CPC][LPC]: per-lane sums over its states
     static constexpr int o_tb = o_ta + 4 * F * CPC * LPC;    // float2 [F][TR]: per-(channel, state) dB, dC terms
-    static constexpr size_t bytes = (size_t)(o_tb + 2 * F * TR) * 4;
+    static constexpr int o_bias = o_tb + 2 * F * TR;         // float [CPC]: dt_bias of the CTA's channels
+    static constexpr size_t bytes = (size_t)(o_bias + CPC) * 4;
     // per-thread shares of the cooperative loops
     static constexpr int PER_T = CPC * kChunk / NT;           // (step, channel) items per thread
     static constexpr int BC_T = kChunk * NP / NT;             // (step, state) items per thread
@@ -107,12 +108,28 @@ struct Shape {
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + ex2(-v * kLog2e)); }
 
 // The raw inputs of one chunk, as each thread loads them (prefetched one
-// chunk ahead into registers).
+// chunk ahead into registers) and unconverted: a float's bits, or a bf16 in
+// the low half.  Nothing in the block that issues the loads uses a loaded
+// value -- addresses outside the problem are clamped to element 0 instead of
+// predicating the load, and the conversion, the zero outside the problem and
+// dt_bias are applied when the chunk is processed -- so the warp never waits
+// for the prefetch where it issues it.
 template <int NP>
 struct Raw {
-    float x[Shape<NP>::PER_T], v[Shape<NP>::PER_T], dy[Shape<NP>::PER_T], z[Shape<NP>::PER_T];
-    float B[Shape<NP>::BC_T], C[Shape<NP>::BC_T];
+    uint32_t x[Shape<NP>::PER_T], v[Shape<NP>::PER_T], dy[Shape<NP>::PER_T], z[Shape<NP>::PER_T];
+    uint32_t B[Shape<NP>::BC_T], C[Shape<NP>::BC_T];
 };
+
+template <typename T> __device__ __forceinline__ uint32_t ld_bits(const void *p, int64_t i);
+template <> __device__ __forceinline__ uint32_t ld_bits<float>(const void *p, int64_t i) {
+    return __float_as_uint(__ldg(static_cast<const float *>(p) + i));
+}
+template <> __device__ __forceinline__ uint32_t ld_bits<__nv_bfloat16>(const void *p, int64_t i) {
+    return (uint32_t)__ldg(static_cast<const unsigned short *>(p) + i);
+}
+template <typename T> __device__ __forceinline__ float of_bits(uint32_t b) {
+    return sizeof(T) == 4 ? __uint_as_float(b) : __uint_as_float(b << 16);
+}
 
 template <typename T, int NP>
 __device__ __forceinline__ void load_raw(const BwdArgs &p, int b, int d0, int k, Raw<NP> &r) {
@@ -124,25 +141,19 @@ __device__ __forceinline__ void load_raw(const BwdArgs &p, int b, int d0, int k,
         const int e = threadIdx.x + i * Sh::NT;          // consecutive threads: consecutive steps
         const int c = e / kChunk, j = e % kChunk;
         const int dd = d0 + c;
-        r.x[i] = r.v[i] = r.dy[i] = r.z[i] = 0.0f;
-        if (dd < p.dim && j < jn) {
-            const int64_t idx = ((int64_t)b * p.dim + dd) * p.L + t0 + j;
-            r.x[i] = Io<T>::ld(p.x, idx);
-            r.v[i] = Io<T>::ld(p.delta, idx) + (p.dt_bias ? __ldg(p.dt_bias + dd) : 0.0f);
-            r.dy[i] = Io<T>::ld(p.dy, idx);
-            if (p.z) r.z[i] = Io<T>::ld(p.z, idx);
-        }
+        const int64_t idx = (dd < p.dim && j < jn) ? ((int64_t)b * p.dim + dd) * p.L + t0 + j : 0;
+        r.x[i] = ld_bits<T>(p.x, idx);
+        r.v[i] = ld_bits<T>(p.delta, idx);
+        r.dy[i] = ld_bits<T>(p.dy, idx);
+        r.z[i] = p.z ? ld_bits<T>(p.z, idx) : 0u;
     }
 #pragma unroll
     for (int i = 0; i < Sh::BC_T; ++i) {
         const int e = threadIdx.x + i * Sh::NT;
         const int n = e / kChunk, j = e % kChunk;
-        r.B[i] = r.C[i] = 0.0f;
-        if (n < p.N && j < jn) {
-            const int64_t idx = ((int64_t)b * p.N + n) * p.L + t0 + j;
-            r.B[i] = Io<T>::ld(p.B, idx);
-            r.C[i] = Io<T>::ld(p.C, idx);
-        }
+        const int64_t idx = (n < p.N && j < jn) ? ((int64_t)b * p.N + n) * p.L + t0 + j : 0;
+        r.B[i] = ld_bits<T>(p.B, idx);
+        r.C[i] = ld_bits<T>(p.C, idx);
     }
 }
 
@@ -172,6 +183,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
     float2 *bc = reinterpret_cast<float2 *>(sm + Sh::o_bc);   // [kChunk][BR]
     float4 *ta = reinterpret_cast<float4 *>(sm + Sh::o_ta);   // [F][CPC][LPC]
     float2 *tb = reinterpret_cast<float2 *>(sm + Sh::o_tb);   // [F][TR]
+    float *sbias = sm + Sh::o_bias;                            // [CPC]
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int li = lane % LPC;
@@ -203,6 +215,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
         dAacc[s] = 0.0f;
     }
     float sum_dD = 0.0f, sum_db = 0.0f;              // this thread's share of dD, ddt_bias (channel rc)
+    if (tid < CPC) sbias[tid] = (p.dt_bias && d0 + tid < dim) ? __ldg(p.dt_bias + d0 + tid) : 0.0f;
+    __syncthreads();
 
     // this CTA's segment: chunks k_lo .. k_hi - 1
     const int k_lo = blockIdx.z * p.seg_chunks;
@@ -220,14 +234,15 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
 #pragma unroll
         for (int i = 0; i < Sh::PER_T; ++i) {
             const int e = tid + i * NT;                     // = channel * kChunk + j
-            const float v = raw.v[i], xx = raw.x[i], g = raw.dy[i];
-            // past the sequence or the channels the step is the identity:
-            // Delta = 0 (softplus of the zero-filled input would be ln 2)
+            // past the sequence or the channels every input is zero and the
+            // step is the identity: Delta = 0 (softplus(0) would be ln 2)
             const bool valid = d0 + e / kChunk < dim && e % kChunk < jn;
+            const float v = valid ? of_bits<T>(raw.v[i]) + sbias[e / kChunk] : 0.0f;
+            const float xx = valid ? of_bits<T>(raw.x[i]) : 0.0f, g = valid ? of_bits<T>(raw.dy[i]) : 0.0f;
             const float dl = !valid ? 0.0f : p.softplus ? softplus2(make_float2(v, v)).x : v;
             float dq = g, zp = 0.0f;
             if (has_z) {
-                const float zz = raw.z[i];
+                const float zz = valid ? of_bits<T>(raw.z[i]) : 0.0f;
                 const float sg = sigmoid_f(zz);
                 dq = g * zz * sg;
                 zp = g * (sg + zz * sg * (1.0f - sg));
@@ -238,7 +253,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
 #pragma unroll
         for (int i = 0; i < Sh::BC_T; ++i) {
             const int e = tid + i * NT;                     // = n * kChunk + j
-            bc[(e % kChunk) * BR + e / kChunk] = make_float2(raw.B[i], raw.C[i]);
+            const bool ok = e / kChunk < N && e % kChunk < jn;
+            bc[(e % kChunk) * BR + e / kChunk] =
+                ok ? make_float2(of_bits<T>(raw.B[i]), of_bits<T>(raw.C[i])) : make_float2(0.0f, 0.0f);
         }
         float hst[S2];                                      // the chunk's start state
 #pragma unroll
@@ -371,6 +388,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArg
     extern __shared__ __align__(16) float sm[];
     float2 *dd = reinterpret_cast<float2 *>(sm);            // [CPC][IR]: Delta, dq
     float *cs = sm + 2 * CPC * IR;                          // [kChunk][BR]: C
+    float *sbias = cs + kChunk * BR;                        // [CPC]: dt_bias of the CTA's channels
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int li = lane % LPC;
@@ -395,6 +413,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArg
         lam[s] = 0.0f;
     }
     float ssum = 0.0f;
+    if (tid < CPC) sbias[tid] = (p.dt_bias && d0 + tid < dim) ? __ldg(p.dt_bias + d0 + tid) : 0.0f;
+    __syncthreads();
     Raw<NP> raw;
     if (k_hi > k_lo) load_raw<T, NP>(p, b, d0, k_hi - 1, raw);
     for (int k = k_hi - 1; k >= k_lo; --k) {
@@ -403,11 +423,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArg
         for (int i = 0; i < Sh::PER_T; ++i) {
             const int e = tid + i * NT;                     // = channel * kChunk + j
             const bool valid = d0 + e / kChunk < dim && e % kChunk < jn;
-            const float v = raw.v[i], g = raw.dy[i];
+            const float v = valid ? of_bits<T>(raw.v[i]) + sbias[e / kChunk] : 0.0f;
+            const float g = valid ? of_bits<T>(raw.dy[i]) : 0.0f;
             const float dl = !valid ? 0.0f : p.softplus ? softplus2(make_float2(v, v)).x : v;
             float dq = g;
             if (has_z) {
-                const float zz = raw.z[i];
+                const float zz = valid ? of_bits<T>(raw.z[i]) : 0.0f;
                 dq = g * zz * sigmoid_f(zz);
             }
             dd[(e / kChunk) * IR + e % kChunk] = make_float2(dl, dq);
@@ -415,7 +436,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArg
 #pragma unroll
         for (int i = 0; i < Sh::BC_T; ++i) {
             const int e = tid + i * NT;                     // = n * kChunk + j
-            cs[(e % kChunk) * BR + e / kChunk] = raw.C[i];
+            const bool ok = e / kChunk < N && e % kChunk < jn;
+            cs[(e % kChunk) * BR + e / kChunk] = ok ? of_bits<T>(raw.C[i]) : 0.0f;
         }
         __syncthreads();
         if (k > k_lo) load_raw<T, NP>(p, b, d0, k - 1, raw);
@@ -509,7 +531,7 @@ cudaError_t launch_np(BwdArgs a, const Plan &pl, const float *dfinal, char *seg_
         const int64_t nchan = (int64_t)a.batch * a.dim;
         float *q = reinterpret_cast<float *>(seg_ws);
         float *ssum = reinterpret_cast<float *>(seg_ws + r256((size_t)pl.nseg * nchan * a.N * 4));
-        const size_t tb = (size_t)(2 * Sh::CPC * Sh::IR + kChunk * Sh::BR) * 4;
+        const size_t tb = (size_t)(2 * Sh::CPC * Sh::IR + kChunk * Sh::BR + Sh::CPC) * 4;
         adj_totals_kernel<T, NP><<<dim3(gx, (unsigned)a.batch, (unsigned)pl.nseg), kWarps * 32, tb, st>>>(a, q, ssum);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int64_t pairs = nchan * a.N;
