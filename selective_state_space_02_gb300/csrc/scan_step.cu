@@ -58,6 +58,39 @@ template <> struct Quad<__nv_bfloat16> {
     }
 };
 
+// Four consecutive I/O elements as loaded, before conversion (float4, or four
+// bf16 in a uint2), and their conversion: the TMA kernel loads ahead of use
+// and converts only where the values are needed, so that no instruction next
+// to the load waits for it.
+template <typename T> struct QuadRaw;
+template <> struct QuadRaw<float> {
+    using type = float4;
+    static __device__ __forceinline__ float4 ld(const void *p, int64_t i) {
+        return __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i));
+    }
+    static __device__ __forceinline__ float4 cvt(float4 v) { return v; }
+};
+template <> struct QuadRaw<__nv_bfloat16> {
+    using type = uint2;
+    static __device__ __forceinline__ uint2 ld(const void *p, int64_t i) {
+        return __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p) + i));
+    }
+    static __device__ __forceinline__ float4 cvt(uint2 w) {
+        return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    }
+};
+
+// One I/O element as loaded (a float's bits, or a bf16 in the low half) and
+// its conversion.
+template <typename T> __device__ __forceinline__ uint32_t ld_bits(const void *p, int64_t i) {
+    if constexpr (sizeof(T) == 4) return __float_as_uint(__ldg(static_cast<const float *>(p) + i));
+    else return (uint32_t)__ldg(static_cast<const unsigned short *>(p) + i);
+}
+template <typename T> __device__ __forceinline__ float of_bits(uint32_t b) {
+    return sizeof(T) == 4 ? __uint_as_float(b) : __uint_as_float(b << 16);
+}
+
 // Elements n .. n+3 of an [rows][N] array at row `row`, zeros past N.
 template <typename T, bool VEC>
 __device__ __forceinline__ float4 quad(const void *base, int64_t row, int N, int n) {
@@ -206,20 +239,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1) step_tma_kernel(const StepArgs
 
     const int gl = tid % G;
     const int r = (tid * NQ / 8) % NQ;                     // first quad this thread visits
-    // the per-channel inputs (x, delta + dt_bias, z) of a tile, loaded one
-    // tile ahead so that their DRAM latency overlaps the previous tile's work
+    // the per-channel inputs (x, delta, dt_bias, z) of a tile, loaded one
+    // tile ahead so that their DRAM latency overlaps the previous tile's
+    // work: raw bits from addresses clamped into the problem, converted (and
+    // dt_bias added) only when the tile is processed
     struct Inputs {
-        float x, v, z;
+        uint32_t x, dl, z;
+        float bias;
     };
     auto load_inputs = [&](uint32_t kk) -> Inputs {
-        Inputs in{0.0f, 0.0f, 0.0f};
-        const uint32_t ch = (blockIdx.x + kk * stride) * TCH + (uint32_t)(tid / G);
-        if (kk < mine_n && ch < nchan) {
-            const uint32_t d = ch % dim;
-            in.x = Io<T>::ld(p.x, ch);
-            in.v = Io<T>::ld(p.delta, ch) + (p.dt_bias ? __ldg(p.dt_bias + d) : 0.0f);
-            if (p.z) in.z = Io<T>::ld(p.z, ch);
-        }
+        Inputs in;
+        const uint32_t c = (blockIdx.x + kk * stride) * TCH + (uint32_t)(tid / G);
+        const uint32_t ch = (kk < mine_n && c < nchan) ? c : 0u;
+        in.x = ld_bits<T>(p.x, ch);
+        in.dl = ld_bits<T>(p.delta, ch);
+        in.z = p.z ? ld_bits<T>(p.z, ch) : 0u;
+        in.bias = p.dt_bias ? __ldg(p.dt_bias + ch % dim) : 0.0f;
         return in;
     };
     Inputs next = load_inputs(0);
@@ -243,18 +278,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1) step_tma_kernel(const StepArgs
         const bool live = ch < nchan;
         const uint32_t b = live ? ch / dim : 0u;
         const uint32_t d = live ? ch - b * dim : 0u;
-        const float xv = cur.x, v = cur.v, zv = cur.z;
         // A, B and C do not depend on the state: load them before the wait
-        float4 A4[NQ], B4[NQ], C4[NQ];
+        // (b and d are clamped into the problem; dead lanes' results are unused)
+        float4 A4[NQ];
+        typename QuadRaw<T>::type Br[NQ], Cr[NQ];
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
             const int n = gl * S + 4 * ((j + r) % NQ);
-            A4[j] = live ? Quad<float>::ld(p.A, (int64_t)d * N + n) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            B4[j] = live ? Quad<T>::ld(p.B, (int64_t)b * N + n) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            C4[j] = live ? Quad<T>::ld(p.C, (int64_t)b * N + n) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            A4[j] = Quad<float>::ld(p.A, (int64_t)d * N + n);
+            Br[j] = QuadRaw<T>::ld(p.B, (int64_t)b * N + n);
+            Cr[j] = QuadRaw<T>::ld(p.C, (int64_t)b * N + n);
         }
         const bool ok = wait_parity(&full[st], (uint32_t)((k / kStages) & 1), status);
         if (!__syncthreads_and(ok)) { aborted = true; break; }
+        const float xv = of_bits<T>(cur.x), v = of_bits<T>(cur.dl) + cur.bias, zv = of_bits<T>(cur.z);
+        float4 B4[NQ], C4[NQ];
+#pragma unroll
+        for (int j = 0; j < NQ; ++j) {
+            B4[j] = QuadRaw<T>::cvt(Br[j]);
+            C4[j] = QuadRaw<T>::cvt(Cr[j]);
+        }
 
         const float Delta = p.softplus ? softplus2(make_float2(v, v)).x : v;
         const float2 dl2 = make_float2(Delta * kLog2e, Delta * kLog2e);
