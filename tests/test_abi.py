@@ -265,3 +265,17 @@ def test_backward_kernel_count(lib):
     assert f(1, 8, 16, 20) == 2
     assert f(0, 8, 16, 20) == 0 and f(1, 8, 16, 0) == 0
     assert f(1, 8, 65, 20) == -1 and f(-1, 8, 16, 20) == -1
+
+
+def test_backward_chunk_state_route_boundary(lib):
+    """The chunk-start states come from one whole-sequence pass once the fused
+    forward's configuration for the shape has at least 608 consumer warps (one
+    per SM sub-partition), else from the totals pass and carry scan: one kernel
+    more.  At 16 states that configuration goes down to 2 states a lane (4
+    channels a warp); at 64 states a lane holds 16 (8 channels a warp)."""
+    f = lib.ssm_scan_bwd_kernel_count
+    # 16 states: 2432 channels = 608 warps; walks split into segments (+3)
+    assert f(1, 2432, 16, 64) == 5 and f(1, 2428, 16, 64) == 6
+    assert f(2, 1216, 13, 4096) == 5 and f(2, 1214, 13, 4096) == 6   # padded states count like 16
+    # 64 states: 4864 channels = 608 warps; one walk
+    assert f(1, 4864, 64, 64) == 3 and f(1, 4856, 64, 64) == 4

@@ -85,6 +85,7 @@ def _compare(g, ref, dtype):
     ((1, 4880, 16, 100), "f32", True),    # TMA rows, ragged last chunk
     ((2, 2440, 13, 70), "bf16", False),   # rows not 16-byte aligned (element loads), padded states
     ((1, 5120, 64, 40), "bf16", True),    # 64 states: 16-step tiles, a state every other tile
+    ((1, 2440, 16, 96), "f32", True),     # the pass at 2 states a lane; walk split into segments
 ])
 def test_backward_matches_oracle(shape, dtype, gate):
     p = synth.make_problem(*shape, dtype=dtype, gate=gate, seed=400 + shape[2] + shape[3], A_mode="random")
