@@ -34,6 +34,7 @@ SIGNATURES = {
     "ssm_scan_fwd": (_i, list(_FWD_ARGS)),
     "ssm_scan_fwd_variant": (_i, list(_FWD_ARGS) + [_i]),
     "ssm_scan_device_status": (_i, [_vp, _i]),
+    "ssm_scan_selftest_wait_timeout": (_i, [ctypes.c_longlong, _vp]),
     "ssm_scan_fwd_host_buffer_size": (_sz, [_i, _i, _i, _i64, _i, _i, _i, _i, _i, _i]),
     "ssm_scan_fwd_host": (_i, list(_FWD_ARGS) + [_i]),
     "ssm_scan_fwd_noalloc": (_i, list(_FWD_ARGS[:16]) + [_vp]),

@@ -21,19 +21,12 @@ namespace {
 
 constexpr int kSMs = 152;
 
-// Device address of g_scan_status for the current device (looked up once).
+// Device address of g_scan_status on the current device, looked up on every
+// call (a cudaDeviceReset reloads the module, possibly at a new address).
 unsigned int *status_ptr() {
-    static std::mutex mu;
-    static unsigned int *ptrs[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!ptrs[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scan_status) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<unsigned int *>(p);
-    }
-    return ptrs[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scan_status) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int *>(p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -338,6 +331,27 @@ cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspac
     const int wpb = 8;
     segment_carry_kernel<<<(unsigned)((pairs + wpb - 1) / wpb), wpb * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, a.h0,
                                                                                    nchan, a.dim, a.dstate, nseg);
+    return cudaGetLastError();
+}
+
+namespace {
+
+// One thread waits, bounded, on an mbarrier that no thread arrives on and no
+// copy targets; the wait runs out, flags the status word and returns.
+__global__ void wait_timeout_kernel(unsigned int *status, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    wait_parity(&bar, 0u, status, limit);
+}
+
+}  // namespace
+
+cudaError_t selftest_wait_timeout(long long limit, cudaStream_t st) {
+    unsigned int *status = status_ptr();
+    if (!status) return cudaErrorInvalidSymbol;
+    wait_timeout_kernel<<<1, 32, 0, st>>>(status, limit);
     return cudaGetLastError();
 }
 

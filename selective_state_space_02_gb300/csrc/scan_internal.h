@@ -50,6 +50,10 @@ int chunk_start_states_kernels(int batch, int dim, int dstate, int64_t L, int64_
 // device (nullptr if the lookup fails); kernels OR bit 0 into it.
 unsigned int *device_status_word();
 
+// Launch the self-test kernel whose bounded wait runs out after `limit` SM
+// cycles and flags the status word.
+cudaError_t selftest_wait_timeout(long long limit, cudaStream_t st);
+
 // Device status word of the bounded waits (bit 0: a wait gave up).  Reads it
 // through `st` (synchronising the stream), optionally clearing it.
 int read_device_status(cudaStream_t st, bool clear, unsigned int *out);

@@ -11,7 +11,7 @@
 // g_noalloc_scratch below, a file-scope __device__ array of
 // kNoAllocScratchBytes (16 MiB) that every GPU loading this library holds
 // until the process exits.
-#include <mutex>
+#include <cstdint>
 
 #include "../../include/ssm_scan.h"
 #include "scan_internal.h"
@@ -25,23 +25,26 @@ constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;   // 16 MiB
 // cudaGetSymbolAddress returns for the current device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached.  Returns nullptr if the
-// lookup fails.
+// Device address of g_noalloc_scratch on the current device, or nullptr if
+// the lookup fails.  It is looked up on every call rather than cached: after
+// a cudaDeviceReset the library's module is loaded again and the array may sit
+// at a new address.  Once the module is loaded on a device the lookup
+// allocates nothing.
 void *scratch_address() {
-    static std::mutex mu;
-    static void *addr[kMaxDevices] = {nullptr};
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
-    }
-    return addr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    return p;
+}
+
+// Whether the fused kernel's scratch for these sizes fits the array.  The
+// first test divides instead of multiplying, so that no product of the sizes
+// can wrap around: every prepared row holds at least 128 bytes per (batch,
+// step).  Past it batch * seqlen is at most 2^17 and the exact size below
+// cannot overflow.
+bool scratch_fits(int batch, int dim, int dstate, int64_t seqlen) {
+    constexpr uint64_t kMinRowBytes = 128;
+    if ((uint64_t)seqlen > kNoAllocScratchBytes / ((uint64_t)batch * kMinRowBytes)) return false;
+    return ssm::fused_workspace_bytes(batch, dim, dstate, seqlen) <= kNoAllocScratchBytes;
 }
 
 }  // namespace
@@ -54,8 +57,7 @@ extern "C" int ssm_scan_fwd_noalloc(const void *x, const void *delta, const floa
     if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64 || seqlen < 0) return SSM_ERR_DIMS;
     // The scratch must hold the fused kernel's B/C rows; reject larger
     // problems before anything touches the GPU.
-    if (batch > 0 && dim > 0 && seqlen > 0 &&
-        ssm::fused_workspace_bytes(batch, dim, dstate, seqlen) > kNoAllocScratchBytes)
+    if (batch > 0 && dim > 0 && seqlen > 0 && !scratch_fits(batch, dim, dstate, seqlen))
         return SSM_ERR_TOO_LARGE;
     void *scratch = nullptr;
     if (batch > 0 && dim > 0 && seqlen > 0) {

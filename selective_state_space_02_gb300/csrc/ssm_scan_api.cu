@@ -311,6 +311,13 @@ int ssm_scan_device_status(void *stream, int clear) {
     return (int)(v & 0x7fffffffu);
 }
 
+int ssm_scan_selftest_wait_timeout(long long limit_cycles, void *stream) {
+    if (limit_cycles < 1 || limit_cycles > (1ll << 31)) return SSM_ERR_DIMS;
+    return ssm::selftest_wait_timeout(limit_cycles, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SSM_OK
+               : SSM_ERR_LAUNCH;
+}
+
 size_t ssm_scan_fwd_host_buffer_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                                      int has_D, int has_z, int has_dt_bias, int has_final_state,
                                      int variant) {
