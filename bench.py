@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "selective-scan Gelem/s (B·D·L/s) and achieved HBM GB/s as % of GB300 roofline"
 UNIT = "Gelem/s"
-DEFAULT_WORKLOAD = "mid_bf16"
+DEFAULT_WORKLOAD = "long_seq_f32"
 SMS = 152                      # GB300 streaming multiprocessors
 SM_MAX_MHZ = 2070.0            # maximum SM clock
 UPDATES_PER_CLK_SM = 32        # (t,d,n) updates per clock per SM: 128 FP32 lanes / 4 ops, 32 ex2/clk
@@ -77,6 +77,7 @@ def parse_args(argv=None):
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed region (clock sampling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-parity", action="store_true", help="skip the all-element check against the oracle")
     ap.add_argument("--op", default="fwd", choices=["fwd", "step", "bwd", "conv"])
     a = ap.parse_args(argv)
     if a.warmup < 3:
@@ -242,16 +243,39 @@ def workload_problem(name: str, rank: int):
     return synth.make_problem(**cfg), cfg
 
 
-def cpu_baseline(p, max_seconds: float = 20.0):
+def _oracle_arrays(p):
+    return dict(x=p.f32("x"), delta=p.f32("delta"), A=p.A.numpy(), B=p.f32("B"), C=p.f32("C"),
+                D=None if p.D is None else p.D.numpy(), z=p.f32("z"),
+                dt_bias=None if p.dt_bias is None else p.dt_bias.numpy())
+
+
+def oracle_full(p):
+    """The fp64 oracle over every channel of the workload on all host cores:
+    (y, final_state, seconds, threads)."""
+    import oracle
+    oracle.build()
+    a = _oracle_arrays(p)
+    threads = oracle.max_threads()
+    t = time.perf_counter()
+    y, fs = oracle.fwd(a["x"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["dt_bias"], p.delta_softplus,
+                       return_final_state=True)
+    return y, fs, time.perf_counter() - t, threads
+
+
+def cpu_baseline(p, max_seconds: float = 20.0, full=None):
     """Time the fp64 oracle on the host cores over a bounded sample of the
-    workload (whole channels, every step)."""
+    workload (whole channels, every step).  ``full`` is a finished pass over
+    the whole workload (from the parity check), used when it stayed within the
+    time bound."""
     import numpy as np
     import oracle
     oracle.build()
     nch = p.batch * p.dim
-    arrs = dict(x=p.f32("x"), delta=p.f32("delta"), A=p.A.numpy(), B=p.f32("B"), C=p.f32("C"),
-                D=None if p.D is None else p.D.numpy(), z=p.f32("z"),
-                dt_bias=None if p.dt_bias is None else p.dt_bias.numpy())
+    if full is not None and full[2] <= 1.5 * max_seconds:
+        dt, threads = full[2], full[3]
+        return {"value": p.elems / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+                "sample": f"whole workload, all {p.seqlen} steps, one pass ({dt:.2f} s)"}
+    arrs = _oracle_arrays(p)
     threads = oracle.max_threads()
     # calibrate on a few channels, then size the sample to ~max_seconds / 2
     probe = list(range(min(nch, max(threads, 8))))
@@ -269,6 +293,29 @@ def cpu_baseline(p, max_seconds: float = 20.0):
     sample = ("whole workload" if k == nch else f"{k} of {nch} channels") + \
         f", all {p.seqlen} steps, one pass ({dt:.2f} s)"
     return {"value": elems / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+
+
+PARITY_TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def parity_check(p, y_dev, fs_dev, full):
+    """Every element of y (and of the final state, when returned) against the
+    oracle: the largest |got - ref| / (1 + |ref|), against the tolerance."""
+    import numpy as np
+    yr, fr = full[0], full[1]
+    nch = p.batch * p.dim
+    yg = y_dev.float().cpu().numpy().reshape(nch, p.seqlen).astype(np.float64)
+    err = float(np.max(np.abs(yg - yr) / (1.0 + np.abs(yr)))) if yr.size else 0.0
+    out = {"oracle": "fp64 CPU recurrence, every element", "elements": int(yr.size),
+           "y_max_scaled_err": err, "y_tol": PARITY_TOL[p.dtype]}
+    ok = err <= PARITY_TOL[p.dtype]
+    if fs_dev is not None:
+        fg = fs_dev.cpu().numpy().reshape(nch, p.dstate).astype(np.float64)
+        ferr = float(np.max(np.abs(fg - fr) / (1.0 + np.abs(fr)))) if fr.size else 0.0
+        out.update({"final_state_max_scaled_err": ferr, "final_state_tol": 1e-4})
+        ok = ok and ferr <= 1e-4
+    out["ok"] = bool(ok)
+    return out
 
 
 # ------------------------------------------------------------- our arm
@@ -380,9 +427,16 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "api": "ssm_scan_fwd_host (pinned host buffers, copies inside the timed region)"}
 
+    full = None
+    parity = None
+    if rank == 0 and (not args.no_parity or (world == 1 and not args.no_cpu_baseline)):
+        full = oracle_full(p)
+    if rank == 0 and not args.no_parity:
+        # rank 0's y (and final state) of the last timed step, checked outside the timed region
+        parity = parity_check(p, y, fs, full)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(p)
+        cpu = cpu_baseline(p, full=full)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -396,6 +450,7 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "parity": parity,
         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
         "gpu_launches": args.steps * KERNELS_PER_STEP[variant],
     }

@@ -180,6 +180,18 @@ int ssm_scan_fwd_from_state(const void *x, const void *delta, const float *A, co
  * word.  Returns the status (>= 0) or SSM_ERR_LAUNCH. */
 int ssm_scan_device_status(void *stream, int clear);
 
+/* Self-test of the bounded waits (the failure detection behind
+ * ssm_scan_device_status).  Launches one small kernel on `stream` whose
+ * thread waits, with the same bounded wait the scan kernels use, on a
+ * shared-memory mbarrier that nothing ever arrives on and that no copy
+ * targets.  After `limit_cycles` SM cycles (1 .. 2^31) the wait gives up, sets
+ * bit 0 of the device status word and the kernel returns normally, so the
+ * context stays usable.  The caller then reads (and clears) the word with
+ * ssm_scan_device_status.  Returns SSM_OK, SSM_ERR_DIMS for a limit out of
+ * range or SSM_ERR_LAUNCH.  Sets the status word shared by every call on the
+ * device: run it only while no scan is in flight. */
+int ssm_scan_selftest_wait_timeout(long long limit_cycles, void *stream);
+
 /* Device bytes that ssm_scan_fwd_host needs as `device_buffer`: room for the
  * device copies of every input and output, the state carried between time
  * chunks and the largest workspace a chunk needs, each 256-byte aligned.
@@ -229,14 +241,19 @@ int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const vo
  *   Limit: batch * seqlen * (2 * padded dstate + 16) * 4 bytes (rounded up to
  *   256) must not exceed 16 MiB, padded dstate = 8, 16, 32 or 64; larger
  *   problems return SSM_ERR_TOO_LARGE before anything is launched.
- *   Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   Set-up: every call looks up the array's device address on the current
+ *   device (cudaGetSymbolAddress).  With CUDA's lazy module loading the first
+ *   call on a device may be the one that loads the library's module there,
+ *   which reserves the 16 MiB array at that moment (and can fail or
+ *   synchronise like any module load); later calls allocate nothing.  Make
+ *   that first call before any stream capture, for example once at start-up.
+ *   After cudaDeviceReset the next call finds the array at its new address.
  *   Sharing: all calls on a device use the same array.  Each call rewrites
  *   the part it reads, so no clearing is needed between calls, but calls that
  *   overlap on the GPU (different streams, no ordering) race on it and must
  *   be serialised by the caller.
- * Allocates no memory, host or device; calls no allocating CUDA routine.
+ * Beyond the first call's module load described above, allocates no memory,
+ * host or device, and calls no allocating CUDA routine.
  */
 int ssm_scan_fwd_noalloc(const void *x, const void *delta, const float *A, const void *B,
                          const void *C, const float *D, const void *z, const float *dt_bias,

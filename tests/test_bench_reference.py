@@ -35,3 +35,21 @@ def test_reference_other_ranks_exit_without_work():
     r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_parity_check_on_cpu():
+    """The bench's all-element parity check (host logic): the oracle's own
+    output passes, one element moved past the tolerance fails."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    from selective_state_space_02_gb300 import synth
+    p = synth.make_problem(1, 6, 16, 50, dtype="bf16", gate=True, final_state=True, seed=7)
+    full = bench.oracle_full(p)
+    y = torch.from_numpy(full[0].reshape(1, 6, 50)).to(torch.bfloat16)
+    fs = torch.from_numpy(full[1].reshape(1, 6, 16)).float()
+    r = bench.parity_check(p, y, fs, full)
+    assert r["ok"] and r["elements"] == 300 and r["y_max_scaled_err"] <= 2 ** -8
+    y[0, 3, 17] += 1.0
+    r = bench.parity_check(p, y, fs, full)
+    assert not r["ok"] and r["y_max_scaled_err"] > 2e-2
