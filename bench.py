@@ -7,7 +7,7 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--variant auto|fused|chunked|twopass] [--impl ours|reference]
-                  [--op fwd|step|bwd|conv]
+                  [--op fwd|step|bwd|conv|convscan]
 
 ``--op step`` times the single-token decode step (ssm_scan_step) on the
 decode workload instead: one step = one token for every sequence of the
@@ -16,7 +16,9 @@ batch, the state resident in HBM, reported against the HBM roofline.
 reverse walk with chunk recomputation) on the forward workload.
 ``--op conv`` times the causal depthwise convolution + SiLU in front of the
 scan (ssm_conv1d_fwd, 4 taps) on the forward workload's x, against the HBM
-roofline.
+roofline.  ``--op convscan`` times convolution and scan in one call
+(ssm_scan_fwd_conv): the convolution fused into the scan kernel, with the
+separate two-kernel chain timed beside it.
 
 N > 1 runs under torch.distributed.run, one rank per GPU: every rank scans its
 own batch of the same shape (weak scaling, no data-path collective); the
@@ -78,7 +80,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-parity", action="store_true", help="skip the all-element check against the oracle")
-    ap.add_argument("--op", default="fwd", choices=["fwd", "step", "bwd", "conv"])
+    ap.add_argument("--op", default="fwd", choices=["fwd", "step", "bwd", "conv", "convscan"])
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -877,6 +879,108 @@ def run_conv(args):
         dist.destroy_process_group()
 
 
+CONVSCAN_METRIC = ("convolution + selective scan Gelem/s (B·D·L/s), the 4-tap causal conv and SiLU "
+                   "fused into the scan kernel, with the separate two-kernel chain timed beside it")
+
+
+def _timed_steps(step, args, flush, stream, world):
+    """Warm-up, then args.steps steps each after an L2 flush, timed with CUDA
+    events on `stream` (ms per step)."""
+    import torch
+    for _ in range(args.warmup):
+        flush_l2(flush)
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush_l2(flush)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return [a.elapsed_time(b_) for a, b_ in zip(starts, ends)]
+
+
+def run_convscan(args):
+    """The convolution + scan call (ssm_scan_fwd_conv) on the workload's shape
+    with a 4-tap filter: the fused mode is the line's value; the separate mode
+    (ssm_conv1d_fwd into the workspace, then the scan) is timed beside it."""
+    import torch
+    import selective_state_space_02_gb300 as ssm
+    from selective_state_space_02_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    p, cfg = workload_problem(args.workload, rank)
+    g = lambda t: None if t is None else t.to(dev)
+    x, dl, z, B, C, A, D, bias = (g(p.x), g(p.delta), g(p.z), g(p.B), g(p.C), g(p.A), g(p.D), g(p.dt_bias))
+    w, cb = synth.make_conv(p.dim, CONV_WIDTH, seed=cfg["seed"] + 11)
+    w, cb = w.to(dev), cb.to(dev)
+    y = torch.empty_like(x)
+    flush = torch.empty(args.flush_mib << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    per = {}
+    for mode in ("fused", "separate"):
+        wsb = ssm.conv_scan_workspace_size(p.batch, p.dim, p.dstate, p.seqlen, CONV_WIDTH, p.torch_dtype, mode)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+
+        def step(mode=mode, ws=ws):
+            ssm.scan_fwd_conv(x, w, dl, A, B, C, conv_bias=cb, D=D, z=z, dt_bias=bias,
+                              delta_softplus=p.delta_softplus, mode=mode, y=y, workspace=ws)
+
+        if mode == "fused":
+            sampler = ClockSampler(local)
+            sampler.start()
+            t_end = time.time() + args.soak_s
+            while time.time() < t_end:
+                for _ in range(20):
+                    flush_l2(flush)
+                    step()
+                torch.cuda.synchronize()
+            per[mode] = _timed_steps(step, args, flush, stream, world)
+            clocks = sampler.stop()
+        else:
+            per[mode] = _timed_steps(step, args, flush, stream, world)
+        del ws
+    total_ms = max_over_ranks(sum(per["fused"]), world, dev)
+    sep_ms = max_over_ranks(sum(per["separate"]), world, dev)
+    elems = p.elems
+    value = world * elems * args.steps / (total_ms / 1e3) / 1e9
+    updates = elems * p.dstate
+    kern_s = statistics.mean(per["fused"]) / 1e3
+    alu_peak = alu_peak_updates_per_s()
+    line = {
+        "metric": CONVSCAN_METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": p.batch, "dim": p.dim, "dstate": p.dstate,
+                   "seqlen": p.seqlen, "width": CONV_WIDTH, "io_dtype": p.dtype, "gate": p.z is not None,
+                   "mode": "fused", "l2": L2_NOTE.format(mib=args.flush_mib),
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "alu", "achieved": round(updates / kern_s / 1e12, 4),
+                     "peak": round(alu_peak / 1e12, 4), "unit": "Tupdate/s",
+                     "frac": round(updates / kern_s / alu_peak, 4), "traffic": None,
+                     "kernel": "fused conv + scan step (B/C re-layout plus the scan kernel with the convolution)"},
+        "separate": {"ms_per_step": round(sep_ms / args.steps, 5),
+                     "value": round(world * elems * args.steps / (sep_ms / 1e3) / 1e9, 3), "unit": UNIT,
+                     "kernels": "ssm_conv1d_fwd, then the scan (B/C re-layout plus the scan kernel)"},
+        "cpu_baseline": None, "e2e": None,
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "gpu_launches": args.steps * 2,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -887,6 +991,8 @@ def main(argv=None):
         run_bwd(args)
     elif args.op == "conv":
         run_conv(args)
+    elif args.op == "convscan":
+        run_convscan(args)
     else:
         run_ours(args)
 

@@ -50,6 +50,42 @@ int ssm_conv1d_fwd(const void *x, const float *weight, const float *bias, const 
                    void *state_out, int silu, int batch, int dim, int64_t seqlen, int width, int io_dtype,
                    void *stream);
 
+/*
+ * Convolution and scan in one call.  "Mamba (part 2)" sect. 4.1 describes the
+ * fused block: the 1-D convolution and its SiLU feed the selective scan
+ * without the convolution's output going through global memory.  This call
+ * computes, for every channel,
+ *
+ *     xc = ssm_conv1d_fwd(x, conv_weight, conv_bias, conv_state, silu = 1)
+ *     y  = the selective scan of ssm_scan_fwd with xc as its input x
+ *
+ * (the D skip uses xc).  Scan arguments, layouts and errors as in
+ * ssm_scan_fwd (ssm_scan.h), x being the convolution's raw input; conv_weight
+ * [dim, conv_width] float32 (required), conv_bias [dim] float32 and
+ * conv_state [batch, dim, conv_width - 1] io_dtype (optional) as in
+ * ssm_conv1d_fwd; conv_width 1 .. 8.  The final state is the scan's.
+ *   mode SSM_CONV_FUSED   : the convolution runs inside the FUSED scan
+ *                           kernel; its output stays in float32 registers
+ *                           (never rounded to io_dtype).  conv_width <= 4,
+ *                           else SSM_ERR_UNSUPPORTED.
+ *   mode SSM_CONV_SEPARATE: ssm_conv1d_fwd writes xc (io_dtype) to the start
+ *                           of the workspace, then the AUTO scan reads it.
+ *   mode SSM_CONV_AUTO    : FUSED when conv_width <= 4 and the scan's AUTO
+ *                           variant for the shape is FUSED, else SEPARATE.
+ * The workspace must hold ssm_scan_fwd_conv_workspace_size(...) bytes
+ * (256-byte aligned; NULL allowed when that is 0).  Asynchronous on `stream`.
+ */
+enum { SSM_CONV_AUTO = -1, SSM_CONV_SEPARATE = 0, SSM_CONV_FUSED = 1 };
+
+size_t ssm_scan_fwd_conv_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int conv_width,
+                                        int io_dtype, int mode);
+
+int ssm_scan_fwd_conv(const void *x, const float *conv_weight, const float *conv_bias, const void *conv_state,
+                      int conv_width, const void *delta, const float *A, const void *B, const void *C,
+                      const float *D, const void *z, const float *dt_bias, int delta_softplus, void *y,
+                      float *final_state, int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                      void *workspace, size_t workspace_bytes, void *stream, int mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,7 @@ import torch
 from . import _native
 from ._native import ScanError, VARIANTS, SSM_BF16, SSM_F32
 
-__all__ = ["scan_fwd", "scan_fwd_host", "scan_step", "scan_bwd", "conv1d", "select_variant", "workspace_size", "ScanError",
+__all__ = ["scan_fwd", "scan_fwd_conv", "conv_scan_workspace_size", "scan_fwd_host", "scan_step", "scan_bwd", "conv1d", "select_variant", "workspace_size", "ScanError",
            "VARIANTS", "host_buffer_size"]
 
 
@@ -142,6 +142,67 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
         rc = lib.ssm_scan_fwd_from_state(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                          _ptr(dt_bias), int(bool(delta_softplus)), _ptr(initial_state),
                                          _ptr(y), fs, batch, dim, N, L, code, ws, ws_bytes, stream, v)
+    _native.check(rc)
+    if return_final_state:
+        return y, final_state
+    return y
+
+
+CONV_MODES = {"auto": -1, "separate": 0, "fused": 1}
+
+
+def conv_scan_workspace_size(batch: int, dim: int, dstate: int, seqlen: int, conv_width: int,
+                             dtype=torch.float32, mode="auto") -> int:
+    n = _native.load().ssm_scan_fwd_conv_workspace_size(batch, dim, dstate, seqlen, conv_width, _dtype_code(dtype),
+                                                        CONV_MODES[mode])
+    if n == (1 << 64) - 1:
+        raise ScanError(-2, "invalid sizes or mode")
+    return n
+
+
+def scan_fwd_conv(x: torch.Tensor, conv_weight: torch.Tensor, delta: torch.Tensor, A: torch.Tensor,
+                  B: torch.Tensor, C: torch.Tensor, conv_bias: Optional[torch.Tensor] = None,
+                  conv_state: Optional[torch.Tensor] = None, D: Optional[torch.Tensor] = None,
+                  z: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+                  delta_softplus: bool = True, return_final_state: bool = False, mode="auto",
+                  y: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None):
+    """Causal depthwise convolution + SiLU of x (include/ssm_conv.h) feeding
+    the forward selective scan, in one call on CUDA tensors.  x is the raw
+    input [batch, dim, L]; conv_weight [dim, width] and conv_bias [dim]
+    float32; conv_state [batch, dim, width-1] in x's dtype (the inputs that
+    preceded the sequence).  ``mode`` "fused" runs the convolution inside the
+    scan kernel (width <= 4), "separate" writes its output to the workspace
+    first, "auto" picks.  Other arguments and the result as in scan_fwd."""
+    batch, dim, N, L = _check_inputs(x, delta, A, B, C, D, z, dt_bias, "cuda")
+    if conv_weight.dtype != torch.float32 or conv_weight.dim() != 2 or conv_weight.shape[0] != dim:
+        raise ValueError("conv_weight must be float32 [dim, width]")
+    width = conv_weight.shape[1]
+    if conv_bias is not None and (conv_bias.dtype != torch.float32 or conv_bias.shape != (dim,)):
+        raise ValueError("conv_bias must be float32 [dim]")
+    if conv_state is not None and (conv_state.dtype != x.dtype or conv_state.shape != (batch, dim, width - 1)):
+        raise ValueError("conv_state must be [batch, dim, width-1] in x's dtype")
+    for name, t in (("conv_weight", conv_weight), ("conv_bias", conv_bias), ("conv_state", conv_state)):
+        if t is not None and (not t.is_contiguous() or t.device.type != "cuda"):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    lib = _native.load()
+    code = _dtype_code(x.dtype)
+    m = CONV_MODES[mode]
+    if y is None:
+        y = torch.empty_like(x)
+    if return_final_state and final_state is None:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=x.device)
+    ws_bytes = lib.ssm_scan_fwd_conv_workspace_size(batch, dim, N, L, width, code, m)
+    if ws_bytes == (1 << 64) - 1:
+        raise ScanError(-8, "this convolution width cannot run fused")
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    rc = lib.ssm_scan_fwd_conv(_ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state), width,
+                               _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                               int(bool(delta_softplus)), _ptr(y),
+                               _ptr(final_state) if return_final_state else None,
+                               batch, dim, N, L, code, _ptr(workspace) if ws_bytes else None, ws_bytes, stream, m)
     _native.check(rc)
     if return_final_state:
         return y, final_state

@@ -44,6 +44,11 @@ SIGNATURES = {
     "ssm_scan_step": (_i, [_vp] * 9 + [_i, _vp, _i, _i, _i, _i, _vp]),
     # x, weight, bias, state_in, y, state_out, silu, batch, dim, seqlen, width, dtype, stream
     "ssm_conv1d_fwd": (_i, [_vp] * 6 + [_i, _i, _i, _i64, _i, _i, _vp]),
+    # batch, dim, dstate, seqlen, width, dtype, mode
+    "ssm_scan_fwd_conv_workspace_size": (_sz, [_i, _i, _i, _i64, _i, _i, _i]),
+    # x, weight, bias, state, width, delta, A, B, C, D, z, dt_bias, softplus, y, final_state,
+    # batch, dim, dstate, seqlen, dtype, workspace, bytes, stream, mode
+    "ssm_scan_fwd_conv": (_i, [_vp] * 4 + [_i] + [_vp] * 7 + [_i, _vp, _vp, _i, _i, _i, _i64, _i, _vp, _sz, _vp, _i]),
     "ssm_scan_bwd_workspace_size": (_sz, [_i, _i, _i, _i64, _i]),
     "ssm_scan_bwd_kernel_count": (_i, [_i, _i, _i, _i64]),
     # x, delta, A, B, C, D, z, dt_bias, softplus, h0, dy, dfinal, dx, ddelta, dA, dB, dC, dD, dz, ddt_bias,

@@ -58,7 +58,25 @@ int max_cfg(int np) { return np == 16 ? 3 : np == 64 ? 0 : 1; }
 // Configuration of the two-pass variant: segments supply the parallelism, and
 // four states per lane (two for N <= 8, eight for N <= 32, sixteen for N <= 64)
 // measured fastest for segmented runs.
-int twopass_cfg(int np) { return np == 16 ? 2 : np == 64 ? 0 : 1; }
+int twopass_cfg(int np) {
+#ifdef SSM_TUNE
+    if (const char *e = std::getenv("SSM_TWOPASS_CFG")) {
+        const int c = std::atoi(e);
+        return c < 0 ? 0 : c > max_cfg(np) ? max_cfg(np) : c;
+    }
+#endif
+    return np == 64 ? 0 : 1;
+}
+
+// Consumer warps per SM that the segment plan of the two-pass variant aims
+// for.  Measured on GB300 with the long-sequence workload (768 channels, 16
+// states, 131072 steps, float32): 8 states a lane with 8 warps per SM (25
+// segments) took 0.82 ms, against 0.95 ms for 4 states a lane and 1.28 ms for
+// 16; plans of 6, 9 or 12 warps per SM were 25-40% slower (partial waves).
+int resident_warps(int np, int cfg) {
+    const int S = fused_states(np, cfg, true);
+    return S >= 16 ? 9 : 8;
+}
 
 // Channels per warp (the TMA box height of x, delta and z).
 int warp_channels(int np, int cfg, bool tma) { return 32 / (np / fused_states(np, cfg, tma)); }
@@ -206,9 +224,13 @@ int64_t twopass_chunk_len(int batch, int dim, int dstate, int64_t L) {
     // (4 resident CTAs: rounding up would leave a second, nearly empty wave),
     // while each segment keeps at least 8 tiles of work.
     const int np = padded_states(dstate);
-    const int cpw = warp_channels(np, twopass_cfg(np), true);
+    const int cfg = twopass_cfg(np);
+    const int cpw = warp_channels(np, cfg, true);
     const int64_t warps = (int64_t)batch * ((dim + cpw - 1) / cpw);
-    const int64_t want = (int64_t)kSMs * 8;
+    int64_t want = (int64_t)kSMs * resident_warps(np, cfg);
+#ifdef SSM_TUNE
+    if (const char *e = std::getenv("SSM_TWOPASS_WANT")) want = (int64_t)kSMs * std::atoi(e);
+#endif
     int64_t nseg = want / (warps > 0 ? warps : 1);
     const int64_t tcs = fused::tile_steps(np);
     const int64_t max_seg = (L + 8 * tcs - 1) / (8 * tcs);
@@ -241,10 +263,7 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
     char *ws = static_cast<char *>(workspace);
     fused::SegArgs sg{len, nseg, reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes),
                       reinterpret_cast<const float *>(ws + hbytes + sbytes)};
-    int cfg = twopass_cfg(padded_states(a.dstate));
-#ifdef SSM_TUNE
-    cfg = choose_cfg(nchan, padded_states(a.dstate), nseg);
-#endif
+    const int cfg = twopass_cfg(padded_states(a.dstate));
     cudaError_t e = cudaSuccess;
     bool prepared = false;
     if (nseg > 1) {   // pass 1 over every segment but the last (its total is never used)

@@ -18,6 +18,9 @@ cudaError_t by_mode(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, u
     const bool gate = a.z != nullptr;
     switch (mode) {
         case kWhole:
+            if (a.conv_k > 0)   // causal convolution (up to 4 taps) fused in front of the scan
+                return gate ? launch_one<T, NP, S, NW, true, kWhole, TMA, 4>(a, sg, maps, status, st)
+                            : launch_one<T, NP, S, NW, false, kWhole, TMA, 4>(a, sg, maps, status, st);
             return gate ? launch_one<T, NP, S, NW, true, kWhole, TMA>(a, sg, maps, status, st)
                         : launch_one<T, NP, S, NW, false, kWhole, TMA>(a, sg, maps, status, st);
         case kTotals:

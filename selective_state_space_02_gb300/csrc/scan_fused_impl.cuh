@@ -95,7 +95,8 @@ struct TileMaps {
 
 __host__ __device__ constexpr size_t align128(size_t n) { return (n + 127) / 128 * 128; }
 
-template <typename T, int NP, int S, int NW, bool GATE, int MODE>
+// CK: taps of the causal convolution fused in front of the scan (0: none).
+template <typename T, int NP, int S, int NW, bool GATE, int MODE, int CK = 0>
 struct Layout {
     static constexpr int NS = NP / S;            // lanes per channel
     static constexpr int CPW = 32 / NS;          // channels per consumer warp
@@ -116,7 +117,11 @@ struct Layout {
     static constexpr size_t off_bc = off_z + (kZ ? align128(row_bytes) : 0);
     static constexpr size_t stage_bytes = off_bc + align128(bc_bytes);
     static constexpr uint32_t tx_bytes = (uint32_t)(row_bytes * (kZ ? 3 : 2) + bc_bytes);
-    static constexpr size_t off_bar = kNST * stage_bytes;
+    // convolution history: the last CK raw inputs of every channel before the
+    // current tile (float, [DT][CK])
+    static constexpr size_t off_halo = kNST * stage_bytes;
+    static constexpr size_t halo_bytes = CK > 0 ? align128((size_t)DT * CK * 4) : 0;
+    static constexpr size_t off_bar = off_halo + halo_bytes;
     static constexpr size_t bytes = off_bar + 2 * kNST * 8 + 16;
 };
 
@@ -291,10 +296,11 @@ struct ReduceScatter<LEN, 0> {
     static __device__ __forceinline__ void run(float (&)[NV], int) {}
 };
 
-template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA>
+template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA, int CK = 0>
 __global__ void __launch_bounds__((NW + 1) * 32, 1)
 scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps maps, unsigned int *status) {
-    using Ly = Layout<T, NP, S, NW, GATE, MODE>;
+    using Ly = Layout<T, NP, S, NW, GATE, MODE, CK>;
+    static_assert(CK == 0 || (MODE == kWhole && CK <= 4), "the convolution runs with whole sequences");
     constexpr int NS = Ly::NS, CPW = Ly::CPW, DT = Ly::DT, E = Ly::E, TC = Ly::TC;
     constexpr bool kY = Ly::kY, kZ = Ly::kZ;
     static_assert(S % 2 == 0 && (NS == 1 || NS == 2 || NS == 4 || NS == 8), "lane split");
@@ -419,6 +425,32 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
     }
     const float bias = (dok && p.dt_bias) ? __ldg(p.dt_bias + d) : 0.0f;
     const float Dd = (dok && p.D) ? __ldg(p.D + d) : 0.0f;
+    // fused convolution: the filter right-aligned in CK taps (zero taps in
+    // front for narrower filters), and the history before the sequence
+    float cw4[CK > 0 ? CK : 1];
+    float cbias = 0.0f;
+    float *halo = reinterpret_cast<float *>(smem + Ly::off_halo) + cl * (CK > 0 ? CK : 1);
+    if constexpr (CK > 0) {
+        const int K = p.conv_k;
+#pragma unroll
+        for (int j = 0; j < CK; ++j) {
+            const int i = j - (CK - K);               // tap index of the filter
+            cw4[j] = (dok && i >= 0) ? __ldg(p.conv_w + (int64_t)d * K + i) : 0.0f;
+        }
+        cbias = (dok && p.conv_b) ? __ldg(p.conv_b + d) : 0.0f;
+        if (g == 0) {
+            // halo[m] holds the raw input at step m - CK of the current tile
+#pragma unroll
+            for (int m = 0; m < CK; ++m) {
+                const int i = m - (CK - (K - 1));     // index into the K-1 inputs before t = 0
+                float v = 0.0f;
+                if (dok && p.conv_state && i >= 0)
+                    v = Io<T>::ld(p.conv_state, (chan0 + d) * (int64_t)(K - 1) + i);
+                halo[m] = v;
+            }
+        }
+        __syncwarp();
+    }
     const bool vec = p.vec16 != 0;
     const bool sp = p.softplus != 0;
     float dsum = 0.0f;
@@ -455,6 +487,37 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
                 float dv[E];
                 rawE<T, E>(base + Ly::off_dl, cl * TC + ce, dv);
                 rawE<T, E>(base + Ly::off_x, cl * TC + ce, xv);
+                if constexpr (CK > 0) {
+                    // x = silu(bias + sum_j w_j raw_{t-CK+1+j}): the lane's E raw
+                    // inputs and the CK-1 before them (from the tile, or for
+                    // the first steps of a tile from the history)
+                    float win[E + CK - 1];
+#pragma unroll
+                    for (int k = 0; k < E; ++k) win[CK - 1 + k] = xv[k];
+#pragma unroll
+                    for (int i = 1; i < CK; ++i) {
+                        const int c = ce - i;          // both reads stay in bounds
+                        const float tv = raw1<T>(base + Ly::off_x, cl * TC + (c >= 0 ? c : 0));
+                        const float hv = halo[CK + (c < 0 ? c : -1)];
+                        win[CK - 1 - i] = c >= 0 ? tv : hv;
+                    }
+#pragma unroll
+                    for (int k = 0; k < E; ++k) {
+                        float acc = cbias;
+#pragma unroll
+                        for (int j = 0; j < CK; ++j) acc = fmaf(cw4[j], win[k + j], acc);
+                        xv[k] = dok ? gate<T>(acc) : 0.0f;
+                    }
+                    if (blk == TC / KB - 1) {
+                        // the tile's last CK raw inputs become the next tile's history
+                        __syncwarp();
+                        if (g == NS - 1) {
+#pragma unroll
+                            for (int m = 0; m < CK; ++m) halo[m] = win[E - 1 + m];
+                        }
+                        __syncwarp();
+                    }
+                }
 #pragma unroll
                 for (int k = 0; k < E; k += 2) {
                     const float2 v = __fadd2_rn(make_float2(dv[k], dv[k + 1]), make_float2(bias, bias));
@@ -580,11 +643,11 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
 }
 
 // Launch one instantiation.
-template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA>
+template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA, int CK = 0>
 cudaError_t launch_one(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, unsigned int *status,
                        cudaStream_t st) {
-    using Ly = Layout<T, NP, S, NW, GATE, MODE>;
-    auto kern = scan_kernel<T, NP, S, NW, GATE, MODE, TMA>;
+    using Ly = Layout<T, NP, S, NW, GATE, MODE, CK>;
+    auto kern = scan_kernel<T, NP, S, NW, GATE, MODE, TMA, CK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ly::bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.dim + Ly::DT - 1) / Ly::DT), (unsigned)a.batch, (unsigned)sg.nseg);

@@ -28,6 +28,12 @@ struct FwdArgs {
     int bf16;              // 1: io elements are bf16, 0: float32
     int vec16;             // 1: every io row starts 16-byte aligned
     const float *h0 = nullptr;   // nullable start state [batch, dim, dstate]; zeros if null
+    // causal depthwise convolution + SiLU fused in front of the scan (FUSED
+    // variant, whole sequences): x is then the raw input, conv_k taps (1..4)
+    int conv_k = 0;
+    const float *conv_w = nullptr;       // [dim, conv_k]
+    const float *conv_b = nullptr;       // nullable [dim]
+    const void *conv_state = nullptr;    // nullable [batch, dim, conv_k - 1], io dtype: inputs before t = 0
 };
 
 // Each launcher returns cudaSuccess or the launch error.

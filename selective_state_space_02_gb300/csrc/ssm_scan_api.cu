@@ -1,6 +1,7 @@
 // C ABI of libssmscan: argument validation, variant selection and the
 // device- and host-buffer entry points.  Declared in include/ssm_scan.h.
 #include "../../include/ssm_scan.h"
+#include "../../include/ssm_conv.h"
 #include "scan_internal.h"
 
 #include <cstring>
@@ -8,7 +9,8 @@
 
 namespace {
 
-constexpr int kVersion = (1 << 16) | 0;
+constexpr int kVersion = (1 << 16) | 1;
+constexpr int kFusedConvTaps = 4;   // widest filter the fused kernel takes
 
 bool valid_sizes(int batch, int dim, int dstate, int64_t seqlen) {
     return batch >= 0 && dim >= 0 && dstate >= 1 && dstate <= 64 && seqlen >= 0;
@@ -227,12 +229,23 @@ size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqle
 
 namespace {
 
-// The device-buffer forward behind ssm_scan_fwd_variant and
-// ssm_scan_fwd_from_state; h0 is the nullable start state.
+// Causal convolution fused in front of the scan (ssm_scan_fwd_conv, fused
+// mode): filter, bias and history; conv_k = 0 means none.
+struct ConvArgs {
+    int conv_k = 0;
+    const float *w = nullptr;
+    const float *b = nullptr;
+    const void *state = nullptr;
+};
+
+// The device-buffer forward behind ssm_scan_fwd_variant,
+// ssm_scan_fwd_from_state and ssm_scan_fwd_conv; h0 is the nullable start
+// state.
 int fwd_device(const void *x, const void *delta, const float *A, const void *B, const void *C, const float *D,
                const void *z, const float *dt_bias, int delta_softplus, const float *h0, void *y,
                float *final_state, int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
-               void *workspace, size_t workspace_bytes, void *stream, int variant) {
+               void *workspace, size_t workspace_bytes, void *stream, int variant,
+               const ConvArgs &conv = ConvArgs{}) {
     int rc = validate(x, delta, A, B, C, D, z, dt_bias, y, final_state, batch, dim, dstate, seqlen,
                       io_dtype, h0);
     if (rc != SSM_OK) return rc;
@@ -264,6 +277,11 @@ int fwd_device(const void *x, const void *delta, const float *A, const void *B, 
     for (const void *q : iop)
         if (q && !aligned(q, 16)) v16 = false;
     a.vec16 = v16 ? 1 : 0;
+    a.conv_k = conv.conv_k;
+    a.conv_w = conv.w;
+    a.conv_b = conv.b;
+    a.conv_state = conv.state;
+    if (conv.conv_k > 0 && v != SSM_VARIANT_FUSED) return SSM_ERR_UNSUPPORTED;
     cudaError_t e;
     switch (v) {
         case SSM_VARIANT_FUSED: e = ssm::launch_fused(a, workspace, st); break;
@@ -446,6 +464,99 @@ int ssm_scan_fwd_host(const void *x, const void *delta, const float *A, const vo
     const bool s3 = cudaStreamSynchronize(hs->out) == cudaSuccess;
     if (rc != SSM_OK) return rc;
     return (!fail && s1 && s2 && s3) ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Convolution in front of the scan.
+namespace {
+
+bool conv_fusable(int batch, int dim, int dstate, int64_t seqlen, int io_dtype, int width) {
+    return width <= kFusedConvTaps &&
+           ssm_scan_select_variant(batch, dim, dstate, seqlen, io_dtype) == SSM_VARIANT_FUSED;
+}
+
+int resolve_conv_mode(int batch, int dim, int dstate, int64_t seqlen, int io_dtype, int width, int mode) {
+    if (mode == SSM_CONV_AUTO)
+        return conv_fusable(batch, dim, dstate, seqlen, io_dtype, width) ? SSM_CONV_FUSED : SSM_CONV_SEPARATE;
+    if (mode == SSM_CONV_FUSED) return width <= kFusedConvTaps ? SSM_CONV_FUSED : SSM_ERR_UNSUPPORTED;
+    if (mode == SSM_CONV_SEPARATE) return SSM_CONV_SEPARATE;
+    return SSM_ERR_VARIANT;
+}
+
+size_t conv_out_bytes(int batch, int dim, int64_t seqlen, int io_dtype) {
+    return round256((size_t)batch * dim * (size_t)seqlen * elem_size(io_dtype));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_fwd_conv_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int conv_width,
+                                        int io_dtype, int mode) {
+    if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return (size_t)-1;
+    if (!valid_sizes(batch, dim, dstate, seqlen) || conv_width < 1 || conv_width > 8) return (size_t)-1;
+    const int m = resolve_conv_mode(batch, dim, dstate, seqlen, io_dtype, conv_width, mode);
+    if (m < 0) return (size_t)-1;
+    if (m == SSM_CONV_FUSED) return workspace_for(batch, dim, dstate, seqlen, SSM_VARIANT_FUSED);
+    const int v = resolve_variant(batch, dim, dstate, seqlen, io_dtype, SSM_VARIANT_AUTO);
+    if (batch <= 0 || dim <= 0 || seqlen <= 0) return 0;
+    return conv_out_bytes(batch, dim, seqlen, io_dtype) + workspace_for(batch, dim, dstate, seqlen, v);
+}
+
+int ssm_scan_fwd_conv(const void *x, const float *conv_weight, const float *conv_bias, const void *conv_state,
+                      int conv_width, const void *delta, const float *A, const void *B, const void *C,
+                      const float *D, const void *z, const float *dt_bias, int delta_softplus, void *y,
+                      float *final_state, int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                      void *workspace, size_t workspace_bytes, void *stream, int mode) {
+    int rc = validate(x, delta, A, B, C, D, z, dt_bias, y, final_state, batch, dim, dstate, seqlen, io_dtype);
+    if (rc != SSM_OK) return rc;
+    if (conv_width < 1 || conv_width > 8) return SSM_ERR_DIMS;
+    const int m = resolve_conv_mode(batch, dim, dstate, seqlen, io_dtype, conv_width, mode);
+    if (m < 0) return m;
+    const bool empty = batch == 0 || dim == 0 || seqlen == 0;
+    if (!empty && !conv_weight) return SSM_ERR_NULL;
+    if ((conv_weight && !aligned(conv_weight, 4)) || (conv_bias && !aligned(conv_bias, 4)) ||
+        (conv_state && !aligned(conv_state, elem_size(io_dtype))))
+        return SSM_ERR_ALIGN;
+    if (!empty) {
+        // the outputs must not overlap the convolution's inputs either
+        const size_t nx = (size_t)batch * dim * (size_t)seqlen * elem_size(io_dtype);
+        const Range cin[] = {range_of(conv_weight, (size_t)dim * conv_width * 4),
+                             range_of(conv_bias, conv_bias ? (size_t)dim * 4 : 0),
+                             range_of(conv_state, conv_state ? (size_t)batch * dim * (conv_width - 1) *
+                                                                    elem_size(io_dtype)
+                                                              : 0)};
+        const Range outs[] = {range_of(y, nx),
+                              range_of(final_state, final_state ? (size_t)batch * dim * dstate * 4 : 0)};
+        for (const Range &o : outs)
+            for (const Range &i : cin)
+                if (overlap(o, i)) return SSM_ERR_ALIAS;
+    }
+    const size_t need = ssm_scan_fwd_conv_workspace_size(batch, dim, dstate, seqlen, conv_width, io_dtype, m);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return SSM_ERR_WORKSPACE;
+    if (m == SSM_CONV_FUSED) {
+        ConvArgs cv;
+        cv.conv_k = empty ? 0 : conv_width;
+        cv.w = conv_weight;
+        cv.b = conv_bias;
+        cv.state = conv_state;
+        return fwd_device(x, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, y, final_state, batch, dim,
+                          dstate, seqlen, io_dtype, workspace, workspace_bytes, stream, SSM_VARIANT_FUSED, cv);
+    }
+    // separate: the convolution's output goes to the front of the workspace,
+    // the scan reads it from there
+    if (empty)
+        return fwd_device(x, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, y, final_state, batch, dim,
+                          dstate, seqlen, io_dtype, workspace, workspace_bytes, stream, SSM_VARIANT_AUTO);
+    const size_t xb = conv_out_bytes(batch, dim, seqlen, io_dtype);
+    rc = ssm_conv1d_fwd(x, conv_weight, conv_bias, conv_state, workspace, nullptr, 1, batch, dim, seqlen,
+                        conv_width, io_dtype, stream);
+    if (rc != SSM_OK) return rc;
+    return fwd_device(workspace, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, y, final_state, batch,
+                      dim, dstate, seqlen, io_dtype, static_cast<char *>(workspace) + xb, workspace_bytes - xb,
+                      stream, SSM_VARIANT_AUTO);
 }
 
 }  // extern "C"
