@@ -113,10 +113,13 @@ bool make_maps(const FwdArgs &a, int cfg, const float *bc, fused::TileMaps &m) {
     const uint32_t tc = (uint32_t)fused::tile_steps(np);
     const int S = fused_states(np, cfg, true);
     const int bcw = fused::bc_row(np, S);
-    return encode_tile_map(&m.x, a.x, bf, (uint64_t)rows, L, dt, tc) &&
-           encode_tile_map(&m.dl, a.delta, bf, (uint64_t)rows, L, dt, tc) &&
+    // float32 tiles of 128-byte rows take the 128-byte swizzle (the layout
+    // the kernel reads through tile_byte)
+    const bool sw = !bf && tc * 4 == 128;
+    return encode_tile_map(&m.x, a.x, bf, (uint64_t)rows, L, dt, tc, sw) &&
+           encode_tile_map(&m.dl, a.delta, bf, (uint64_t)rows, L, dt, tc, sw) &&
            encode_f32_map(&m.bc, bc, (uint64_t)brows, (uint64_t)bcw, tc, (uint32_t)bcw) &&
-           (!a.z || encode_tile_map(&m.z, a.z, bf, (uint64_t)rows, L, dt, tc));
+           (!a.z || encode_tile_map(&m.z, a.z, bf, (uint64_t)rows, L, dt, tc, sw));
 }
 
 // Bytes of the prepared B/C rows: [batch * L][widest row] float.
@@ -135,51 +138,101 @@ cudaError_t launch_mode(const FwdArgs &a, const fused::SegArgs &sg, int mode, in
     return fused::launch_typed<float>(a, sg, maps, status, mode, tma, cfg, prepare, st);
 }
 
-// Small scan over the segment totals ("Mamba hardware-aware parallel
-// associative scan", sect. 3.3, second method), one warp per (channel,
-// state): the segment pairs (A_k, B_k) = (exp(A * sum Delta_k), h_end_k) are
-// combined with a warp-shuffle Hillis-Steele scan, 32 segments per round, the
-// running state carried from round to round.  On return ws_h[k] holds the
-// state at the start of segment k, h_init^(k), with h_init^(0) the start state
-// h0 of the whole sequence (zero when h0 is null).
-__global__ void segment_carry_kernel(const float *__restrict__ A, float *ws_h, const float *__restrict__ ws_s,
-                                     const float *__restrict__ h0, int64_t nchan, int dim, int N, int nseg) {
+// Carry over the segment totals ("Mamba hardware-aware parallel associative
+// scan", sect. 3.3): for every (channel, state) pair, in segment order,
+// h_init^(k+1) = A_k h_init^(k) + B_k with the segment's pair (A_k, B_k) =
+// (exp(A * sum Delta_k), its end state from the zero state).  On return
+// ws_h[k] holds the state at the start of segment k, h_init^(0) being the
+// start state h0 of the whole sequence (zero when h0 is null).  The last
+// segment's total is never read (pass 1 does not form it).
+//
+// Two levels, so that every load is coalesced and a long chain of segments
+// still has parallelism: a CTA takes 32 consecutive pairs (lane = pair) and
+// kCarryWarps warps, warp w a contiguous group of the segments.
+//   1. each warp composes its group's pairs into one (A_g, B_g), A_g from the
+//      group's summed Delta (one exponential, the log-domain form);
+//   2. through shared memory each warp composes the groups before its own
+//      with the start state into its group's start;
+//   3. each warp walks its group again from that start, writing the segment
+//      start states.
+constexpr int kCarryWarps = 16;
+
+__global__ void __launch_bounds__(kCarryWarps * 32) segment_carry_kernel(const float *__restrict__ A, float *ws_h,
+                                                                          const float *__restrict__ ws_s,
+                                                                          const float *__restrict__ h0,
+                                                                          int64_t nchan, int dim, int N, int nseg) {
+    __shared__ float gA[kCarryWarps][32], gB[kCarryWarps][32];
     const int lane = threadIdx.x & 31;
-    const int64_t pair = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (pair >= nchan * N) return;                 // whole warp leaves together
-    const int64_t ch = pair / N;
-    const int n = (int)(pair % N);
-    const float a2 = A[(int64_t)(ch % dim) * N + n] * kLog2e;
-    float carry = h0 ? h0[ch * N + n] : 0.0f;       // h_init of the first segment of the round
-    for (int k0 = 0; k0 < nseg; k0 += 32) {
-        const int k = k0 + lane;
-        float Ak = 1.0f, Bk = 0.0f;                 // identity pads the round
-        if (k < nseg - 1) {                         // the last segment's total is never needed
-            Ak = ex2(a2 * ws_s[(int64_t)k * nchan + ch]);
-            Bk = ws_h[((int64_t)k * nchan + ch) * N + n];
-        }
-        // inclusive Hillis-Steele scan over the lanes: x_i <- x_i o x_{i-off}
+    const int w = threadIdx.x >> 5;
+    const int64_t npair = nchan * N;
+    const int64_t pair = (int64_t)blockIdx.x * 32 + lane;
+    const bool ok = pair < npair;
+    const int64_t pc = ok ? pair : 0;               // a valid pair for the loads of idle lanes
+    const int64_t ch = pc / N;
+    const int n = (int)(pc % N);
+    const float a2 = A[(ch % dim) * N + n] * kLog2e;
+    const int per = (nseg + kCarryWarps - 1) / kCarryWarps;
+    const int k0 = w * per;
+    const int k1 = (k0 + per < nseg) ? k0 + per : nseg;
+    const int kt = k1 < nseg - 1 ? k1 : nseg - 1;   // segments of the group that have totals
+    // 1. the group's composition from the zero state (loads issued U segments
+    // ahead of the dependent multiply-adds)
+    constexpr int U = 8;
+    float hg = 0.0f, sg = 0.0f;
+    int k = k0;
+    for (; k + U <= kt; k += U) {
+        float Bv[U], sv[U];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float Ap = __shfl_up_sync(0xffffffffu, Ak, off);
-            const float Bp = __shfl_up_sync(0xffffffffu, Bk, off);
-            if (lane >= off) {
-                Bk = fmaf(Ak, Bp, Bk);
-                Ak = Ak * Ap;
-            }
+        for (int j = 0; j < U; ++j) {
+            Bv[j] = ws_h[(int64_t)(k + j) * npair + pc];
+            sv[j] = ws_s[(int64_t)(k + j) * nchan + ch];
         }
-        const float hend = fmaf(Ak, carry, Bk);     // state after segment k
-        float hstart = __shfl_up_sync(0xffffffffu, hend, 1);
-        if (lane == 0) hstart = carry;
-        if (k < nseg) ws_h[((int64_t)k * nchan + ch) * N + n] = hstart;
-        carry = __shfl_sync(0xffffffffu, hend, 31);
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            hg = fmaf(ex2(a2 * sv[j]), hg, Bv[j]);
+            sg += sv[j];
+        }
+    }
+    for (; k < kt; ++k) {
+        const float sk = ws_s[(int64_t)k * nchan + ch];
+        hg = fmaf(ex2(a2 * sk), hg, ws_h[(int64_t)k * npair + pc]);
+        sg += sk;
+    }
+    gA[w][lane] = ex2(a2 * sg);
+    gB[w][lane] = hg;
+    __syncthreads();
+    // 2. the group's start state
+    float h = (ok && h0) ? h0[pair] : 0.0f;
+    for (int v = 0; v < w; ++v) h = fmaf(gA[v][lane], h, gB[v][lane]);
+    // 3. the segment start states of the group
+    k = k0;
+    for (; k + U <= kt; k += U) {
+        float Bv[U], sv[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            Bv[j] = ws_h[(int64_t)(k + j) * npair + pc];
+            sv[j] = ws_s[(int64_t)(k + j) * nchan + ch];
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            if (ok) ws_h[(int64_t)(k + j) * npair + pc] = h;
+            h = fmaf(ex2(a2 * sv[j]), h, Bv[j]);
+        }
+    }
+    for (; k < k1; ++k) {
+        const int64_t i = (int64_t)k * npair + pc;
+        const bool has = k < nseg - 1;
+        const float Bk = has ? ws_h[i] : 0.0f;
+        const float sk = has ? ws_s[(int64_t)k * nchan + ch] : 0.0f;
+        if (ok) ws_h[i] = h;
+        h = fmaf(ex2(a2 * sk), h, Bk);
     }
 }
 
 }  // namespace
 
 bool encode_tile_map(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows, uint32_t box_cols) {
+                     uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
     auto fn = encode_fn();
     if (!fn) return false;
     const size_t es = bf16 ? 2 : 4;
@@ -187,10 +240,11 @@ bool encode_tile_map(CUtensorMap *map, const void *base, bool bf16, uint64_t row
     cuuint64_t strides[1] = {cols * es};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
+    if (swizzle128 && box_cols * es != 128) return false;
     CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -274,9 +328,8 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
         prepared = true;
     }
     const int64_t pairs = nchan * a.dstate;
-    const int wpb = 8;
-    segment_carry_kernel<<<(unsigned)((pairs + wpb - 1) / wpb), wpb * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, a.h0,
-                                                                                   nchan, a.dim, a.dstate, nseg);
+    segment_carry_kernel<<<(unsigned)((pairs + 31) / 32), kCarryWarps * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, a.h0,
+                                                                                    nchan, a.dim, a.dstate, nseg);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_mode(a, sg, fused::kSeeded, cfg, !prepared, st);
@@ -347,9 +400,8 @@ cudaError_t chunk_start_states(const FwdArgs &a, int64_t seg_len, void *workspac
         if (e != cudaSuccess) return e;
     }
     const int64_t pairs = nchan * a.dstate;
-    const int wpb = 8;
-    segment_carry_kernel<<<(unsigned)((pairs + wpb - 1) / wpb), wpb * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, a.h0,
-                                                                                   nchan, a.dim, a.dstate, nseg);
+    segment_carry_kernel<<<(unsigned)((pairs + 31) / 32), kCarryWarps * 32, 0, st>>>(a.A, sg.ws_h, sg.ws_s, a.h0,
+                                                                                    nchan, a.dim, a.dstate, nseg);
     return cudaGetLastError();
 }
 

@@ -110,20 +110,38 @@ struct Layout {
     static constexpr size_t row_bytes = (size_t)DT * TC * sizeof(T);
     static constexpr int BCW = bc_row(NP, S);    // floats per prepared B/C row
     static constexpr size_t bc_bytes = (size_t)TC * BCW * 4;
+    // float32 tiles of 128-byte rows are copied with the 128-byte swizzle
+    // (tile_byte); their buffers start on 1024-byte boundaries
+    static constexpr bool kSW = sizeof(T) == 4 && TC * 4 == 128;
+    static constexpr size_t kAl = kSW ? 1024 : 128;
+    static constexpr size_t al(size_t n) { return (n + kAl - 1) / kAl * kAl; }
     // one ring stage
     static constexpr size_t off_x = 0;
-    static constexpr size_t off_dl = align128(row_bytes);
-    static constexpr size_t off_z = off_dl + align128(row_bytes);
-    static constexpr size_t off_bc = off_z + (kZ ? align128(row_bytes) : 0);
-    static constexpr size_t stage_bytes = off_bc + align128(bc_bytes);
+    static constexpr size_t off_dl = al(row_bytes);
+    static constexpr size_t off_z = off_dl + al(row_bytes);
+    static constexpr size_t off_bc = off_z + (kZ ? al(row_bytes) : 0);
+    static constexpr size_t stage_bytes = off_bc + al(bc_bytes);
     static constexpr uint32_t tx_bytes = (uint32_t)(row_bytes * (kZ ? 3 : 2) + bc_bytes);
     // convolution history: the last CK raw inputs of every channel before the
     // current tile (float, [DT][CK])
     static constexpr size_t off_halo = kNST * stage_bytes;
     static constexpr size_t halo_bytes = CK > 0 ? align128((size_t)DT * CK * 4) : 0;
     static constexpr size_t off_bar = off_halo + halo_bytes;
-    static constexpr size_t bytes = off_bar + 2 * kNST * 8 + 16;
+    // (plus room to align the base of a swizzled layout)
+    static constexpr size_t bytes = off_bar + 2 * kNST * 8 + 16 + (kSW ? 1024 : 0);
 };
+
+// Byte offset of element (row r, column c) of a staged x, delta or z tile of
+// TC columns.  With the 128-byte swizzle (rows of exactly 128 bytes, tile on
+// a 1024-byte boundary) the copy stores a row's 16-byte chunk j at chunk
+// j ^ (r mod 8), so that the same column of eight consecutive rows falls in
+// eight different bank groups.
+template <typename T, int TC, bool SW>
+__device__ __forceinline__ int tile_byte(int r, int c) {
+    const int off = (r * TC + c) * (int)sizeof(T);
+    if constexpr (SW) return off ^ ((r & 7) << 4);
+    return off;
+}
 
 // Raw tile element access (shared memory).
 template <typename T>
@@ -178,6 +196,36 @@ __device__ __forceinline__ void rawE(const unsigned char *base, int idx, float (
             v[0] = raw1<T>(base, idx);
         }
     }
+}
+
+// E consecutive elements of row r from column c (c * sizeof(T) aligned to
+// min(E * sizeof(T), 16)) of a staged tile; every 16-byte chunk is contiguous
+// in the swizzled layout too.
+template <typename T, int E, int TC, bool SW>
+__device__ __forceinline__ void rowE(const unsigned char *tile, int r, int c, float (&v)[E]) {
+    if constexpr (!SW) {
+        rawE<T, E>(tile, r * TC + c, v);
+    } else {
+        static_assert(sizeof(T) == 4, "swizzled tiles are float32");
+        if constexpr (E % 4 == 0) {
+#pragma unroll
+            for (int k = 0; k < E; k += 4) {
+                const float4 q = *reinterpret_cast<const float4 *>(tile + tile_byte<T, TC, SW>(r, c + k));
+                v[k] = q.x; v[k + 1] = q.y; v[k + 2] = q.z; v[k + 3] = q.w;
+            }
+        } else if constexpr (E == 2) {
+            const float2 q = *reinterpret_cast<const float2 *>(tile + tile_byte<T, TC, SW>(r, c));
+            v[0] = q.x; v[1] = q.y;
+        } else {
+            v[0] = *reinterpret_cast<const float *>(tile + tile_byte<T, TC, SW>(r, c));
+        }
+    }
+}
+
+template <typename T, int TC, bool SW>
+__device__ __forceinline__ float row1(const unsigned char *tile, int r, int c) {
+    if constexpr (!SW) return raw1<T>(tile, r * TC + c);
+    return *reinterpret_cast<const float *>(tile + tile_byte<T, TC, SW>(r, c));
 }
 
 // Store E consecutive outputs at global index idx (all in range).
@@ -308,7 +356,10 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
     static_assert(E % 2 == 0 && TC % KB == 0, "block split");
     constexpr unsigned FULL = 0xffffffffu;
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw;
+    if constexpr (Ly::kSW) smem += (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    constexpr bool SW = Ly::kSW;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Ly::off_bar);
     uint64_t *empty = full + kNST;
     int *abort_flag = reinterpret_cast<int *>(empty + kNST);
@@ -372,9 +423,10 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
                         dv = static_cast<const T *>(p.delta)[idx];
                         if constexpr (kZ) zv = static_cast<const T *>(p.z)[idx];
                     }
-                    reinterpret_cast<T *>(base + Ly::off_x)[e] = xv;
-                    reinterpret_cast<T *>(base + Ly::off_dl)[e] = dv;
-                    if constexpr (kZ) reinterpret_cast<T *>(base + Ly::off_z)[e] = zv;
+                    const int tb = tile_byte<T, TC, SW>(r, c);
+                    *reinterpret_cast<T *>(base + Ly::off_x + tb) = xv;
+                    *reinterpret_cast<T *>(base + Ly::off_dl + tb) = dv;
+                    if constexpr (kZ) *reinterpret_cast<T *>(base + Ly::off_z + tb) = zv;
                 }
                 float *bcs = reinterpret_cast<float *>(base + Ly::off_bc);
                 for (int e = lane; e < TC * Ly::BCW; e += 32) {
@@ -400,7 +452,12 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
 
     // ---------------------------------------------------------------- consumer
     if (warp >= nw_live) return;                       // no channels for this warp
-    const int cw = lane / NS;                           // channel within the warp
+    // channel within the warp; with swizzled tiles and two lanes a channel
+    // the channels are permuted (bits 1 and 2 of the index swapped) so that
+    // a quarter-warp's four channels sit in rows 0, 1, 4, 5 (or 2, 3, 6, 7)
+    // modulo 8 and its 16-byte tile reads fall in eight bank groups
+    const int cw = (SW && NS == 2) ? (((lane / NS) & 9) | (((lane / NS) & 2) << 1) | (((lane / NS) & 4) >> 1))
+                                   : lane / NS;
     const int g = lane % NS;                            // state group
     const int cl = warp * CPW + cw;                     // channel within the CTA
     const int d = d0 + cl;
@@ -485,8 +542,8 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
             float Dl[E], Ul[E], xv[E];
             {
                 float dv[E];
-                rawE<T, E>(base + Ly::off_dl, cl * TC + ce, dv);
-                rawE<T, E>(base + Ly::off_x, cl * TC + ce, xv);
+                rowE<T, E, TC, SW>(base + Ly::off_dl, cl, ce, dv);
+                rowE<T, E, TC, SW>(base + Ly::off_x, cl, ce, xv);
                 if constexpr (CK > 0) {
                     // x = silu(bias + sum_j w_j raw_{t-CK+1+j}): the lane's E raw
                     // inputs and the CK-1 before them (from the tile, or for
@@ -497,7 +554,7 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
 #pragma unroll
                     for (int i = 1; i < CK; ++i) {
                         const int c = ce - i;          // both reads stay in bounds
-                        const float tv = raw1<T>(base + Ly::off_x, cl * TC + (c >= 0 ? c : 0));
+                        const float tv = row1<T, TC, SW>(base + Ly::off_x, cl, c >= 0 ? c : 0);
                         const float hv = halo[CK + (c < 0 ? c : -1)];
                         win[CK - 1 - i] = c >= 0 ? tv : hv;
                     }
@@ -595,7 +652,7 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
                 // ---- skip, gate, store the lane's own steps ---------------------
                 if (dok) {
                     float zv[E];
-                    if constexpr (kZ) rawE<T, E>(base + Ly::off_z, cl * TC + ce, zv);
+                    if constexpr (kZ) rowE<T, E, TC, SW>(base + Ly::off_z, cl, ce, zv);
 #pragma unroll
                     for (int k = 0; k < E; k += 2) {
                         float2 v = __ffma2_rn(make_float2(Dd, Dd), make_float2(xv[k], xv[k + 1]),
