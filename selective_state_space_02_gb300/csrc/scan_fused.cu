@@ -113,9 +113,10 @@ bool make_maps(const FwdArgs &a, int cfg, const float *bc, fused::TileMaps &m) {
     const uint32_t tc = (uint32_t)fused::tile_steps(np);
     const int S = fused_states(np, cfg, true);
     const int bcw = fused::bc_row(np, S);
-    // float32 tiles of 128-byte rows take the 128-byte swizzle (the layout
-    // the kernel reads through tile_byte)
-    const bool sw = !bf && tc * 4 == 128;
+    // tiles of 128-byte rows take the 128-byte swizzle, of 64-byte rows the
+    // 64-byte swizzle (the layouts the kernel reads through tile_byte)
+    const uint32_t rowb = tc * (bf ? 2u : 4u);
+    const int sw = rowb == 128 ? 128 : rowb == 64 ? 64 : 0;
     return encode_tile_map(&m.x, a.x, bf, (uint64_t)rows, L, dt, tc, sw) &&
            encode_tile_map(&m.dl, a.delta, bf, (uint64_t)rows, L, dt, tc, sw) &&
            encode_f32_map(&m.bc, bc, (uint64_t)brows, (uint64_t)bcw, tc, (uint32_t)bcw) &&
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kCarryWarps * 32) segment_carry_kernel(const f
 }  // namespace
 
 bool encode_tile_map(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
+                     uint32_t box_rows, uint32_t box_cols, int swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
     const size_t es = bf16 ? 2 : 4;
@@ -240,10 +241,12 @@ bool encode_tile_map(CUtensorMap *map, const void *base, bool bf16, uint64_t row
     cuuint64_t strides[1] = {cols * es};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    if (swizzle128 && box_cols * es != 128) return false;
+    if (swizzle && box_cols * es != (uint32_t)swizzle) return false;
     CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                    : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

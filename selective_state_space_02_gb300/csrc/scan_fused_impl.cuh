@@ -110,9 +110,11 @@ struct Layout {
     static constexpr size_t row_bytes = (size_t)DT * TC * sizeof(T);
     static constexpr int BCW = bc_row(NP, S);    // floats per prepared B/C row
     static constexpr size_t bc_bytes = (size_t)TC * BCW * 4;
-    // float32 tiles of 128-byte rows are copied with the 128-byte swizzle
-    // (tile_byte); their buffers start on 1024-byte boundaries
-    static constexpr bool kSW = sizeof(T) == 4 && TC * 4 == 128;
+    // tiles of 128-byte rows (float32) are copied with the 128-byte swizzle,
+    // tiles of 64-byte rows (bf16) with the 64-byte swizzle (tile_byte);
+    // their buffers start on 1024-byte boundaries
+    static constexpr int kSWZ = TC * (int)sizeof(T) == 128 ? 128 : TC * (int)sizeof(T) == 64 ? 64 : 0;
+    static constexpr bool kSW = kSWZ != 0;
     static constexpr size_t kAl = kSW ? 1024 : 128;
     static constexpr size_t al(size_t n) { return (n + kAl - 1) / kAl * kAl; }
     // one ring stage
@@ -132,14 +134,18 @@ struct Layout {
 };
 
 // Byte offset of element (row r, column c) of a staged x, delta or z tile of
-// TC columns.  With the 128-byte swizzle (rows of exactly 128 bytes, tile on
-// a 1024-byte boundary) the copy stores a row's 16-byte chunk j at chunk
-// j ^ (r mod 8), so that the same column of eight consecutive rows falls in
-// eight different bank groups.
+// TC columns, the tile on a 1024-byte boundary.  The swizzled copies XOR the
+// 16-byte chunk bits of an offset with the bits above the 128-byte line: the
+// 128-byte mode bits 4-6 with bits 7-9 (a 128-byte row r stores chunk j at
+// j ^ (r mod 8)), the 64-byte mode bits 4-5 with bits 7-8 (a 64-byte row r
+// stores chunk j at j ^ ((r / 2) mod 4)).  The same column of consecutive
+// rows then falls in different bank groups.
 template <typename T, int TC, bool SW>
 __device__ __forceinline__ int tile_byte(int r, int c) {
+    constexpr int row = TC * (int)sizeof(T);
     const int off = (r * TC + c) * (int)sizeof(T);
-    if constexpr (SW) return off ^ ((r & 7) << 4);
+    if constexpr (SW && row == 128) return off ^ (((off >> 7) & 7) << 4);
+    if constexpr (SW && row == 64) return off ^ (((off >> 7) & 3) << 4);
     return off;
 }
 
@@ -205,8 +211,7 @@ template <typename T, int E, int TC, bool SW>
 __device__ __forceinline__ void rowE(const unsigned char *tile, int r, int c, float (&v)[E]) {
     if constexpr (!SW) {
         rawE<T, E>(tile, r * TC + c, v);
-    } else {
-        static_assert(sizeof(T) == 4, "swizzled tiles are float32");
+    } else if constexpr (sizeof(T) == 4) {
         if constexpr (E % 4 == 0) {
 #pragma unroll
             for (int k = 0; k < E; k += 4) {
@@ -219,13 +224,26 @@ __device__ __forceinline__ void rowE(const unsigned char *tile, int r, int c, fl
         } else {
             v[0] = *reinterpret_cast<const float *>(tile + tile_byte<T, TC, SW>(r, c));
         }
+    } else {
+        // bf16: 16-byte chunks of 8 elements, or a piece of one chunk
+        if constexpr (E % 8 == 0) {
+#pragma unroll
+            for (int k = 0; k < E; k += 8) {
+                float w[8];
+                rawE<T, 8>(tile + tile_byte<T, TC, SW>(r, c + k), 0, w);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[k + i] = w[i];
+            }
+        } else {
+            rawE<T, E>(tile + tile_byte<T, TC, SW>(r, c), 0, v);
+        }
     }
 }
 
 template <typename T, int TC, bool SW>
 __device__ __forceinline__ float row1(const unsigned char *tile, int r, int c) {
     if constexpr (!SW) return raw1<T>(tile, r * TC + c);
-    return *reinterpret_cast<const float *>(tile + tile_byte<T, TC, SW>(r, c));
+    return raw1<T>(tile + tile_byte<T, TC, SW>(r, c), 0);
 }
 
 // Store E consecutive outputs at global index idx (all in range).

@@ -106,12 +106,12 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Host: encode a row-major [rows][cols] tensor of `elem` bytes per element,
-// box [box_rows][box_cols], zero fill out of bounds; `swizzle128` selects the
-// 128-byte shared-memory swizzle (box rows of 128 bytes, destinations on
-// 1024-byte boundaries).  Returns false if the driver entry point is
-// unavailable or rejects the map.
+// box [box_rows][box_cols], zero fill out of bounds; `swizzle` 128 or 64
+// selects that shared-memory swizzle (box rows of exactly that many bytes,
+// destinations on 1024-byte boundaries), 0 none.  Returns false if the
+// driver entry point is unavailable or rejects the map.
 bool encode_tile_map(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows, uint32_t box_cols, bool swizzle128 = false);
+                     uint32_t box_rows, uint32_t box_cols, int swizzle = 0);
 
 // Host: the same for a float32 tensor whose rows hold `cols` values.
 bool encode_f32_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
