@@ -147,15 +147,16 @@ def source_hash(variant: str) -> str:
 
 
 def profiled_traffic(workload: str, variant: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    """DRAM bytes per step (all of the step's kernels) from the committed ncu
+    summary, or None when the kernel sources changed since the counters were
+    taken."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             j = json.load(f)
         e = j[workload][variant]
         if e.get("source_hash") != source_hash(variant):
             return None
-        return e["dram_bytes_per_launch"]
+        return e["dram_bytes_per_step"]
     except Exception:
         return None
 
@@ -393,7 +394,12 @@ def run_ours(args):
         "unit": "Tupdate/s",
         "frac": round(alu_achieved / alu_peak, 4),
         "traffic": traffic,
-        "kernel": f"{variant} scan step (B/C re-layout, ~3% of it, plus the scan kernel)" if variant != "chunked" else "chunked scan step (B/C chunk re-layout plus the scan kernel)",
+        "kernel": {"fused": "fused scan step: B/C re-layout (~3%) and the scan kernel",
+                   "twopass": "two-pass scan step: B/C re-layout, totals pass, segment carry, seeded pass "
+                              "(all four launches; achieved and traffic per step)",
+                   "chunked": "chunked scan step: B/C chunk re-layout and the scan kernel"}[variant],
+        "traffic_note": "DRAM bytes of all the step's kernels from one ncu capture; y lines still dirty in L2 "
+                        "when the last kernel ends are written back after it and are not counted",
         "peak_basis": f"{SMS} SMs x {SM_MAX_MHZ:.0f} MHz x {UPDATES_PER_CLK_SM} (t,d,n) updates/clk/SM "
                       "(1 ex2 + 4 FP32 ops per update; 32 ex2 and 128 FP32 lanes per clk per SM)",
         "hbm": {"achieved": round(hbm_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
