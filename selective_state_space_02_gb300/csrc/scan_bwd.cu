@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
         for (int sub = kChunk / SC - 1; sub >= 0; --sub) {
             const int j0 = sub * SC;
             float h[S2][SC + 1];                            // h[s][j + 1] = state after step j0 + j
+            float av[S2][SC];                               // av[s][j] = a of step j0 + j (for the adjoint)
 #pragma unroll
             for (int s = 0; s < S2; ++s) h[s][0] = hst[s];
 #pragma unroll 4
@@ -285,8 +286,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
             for (int j = 0; j < SC; ++j) {
                 const float4 q = in[c * IR + j0 + j];
 #pragma unroll
-                for (int s = 0; s < S2; ++s)
-                    h[s][j + 1] = fmaf(ex2(q.x * A2[s]), h[s][j], q.y * bc[(j0 + j) * BR + li + LPC * s].x);
+                for (int s = 0; s < S2; ++s) {
+                    av[s][j] = ex2(q.x * A2[s]);
+                    h[s][j + 1] = fmaf(av[s][j], h[s][j], q.y * bc[(j0 + j) * BR + li + LPC * s].x);
+                }
             }
             // ---- c. the adjoint backwards, F steps between reductions ----------
 #pragma unroll
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
                         const int n = li + LPC * s;
                         const float2 BC = bc[j * BR + n];
                         lam[s] = fmaf(q.z, BC.y, lam[s]);
-                        const float a = ex2(q.x * A2[s]);
+                        const float a = av[s][jl];
                         const float daa = lam[s] * h[s][jl] * a;     // (dL/da_t) a_t
                         dAacc[s] = fmaf(daa, q.x, dAacc[s]);
                         du = fmaf(lam[s], BC.x, du);
