@@ -207,13 +207,16 @@ int ssm_scan_select_variant(int batch, int dim, int dstate, int64_t seqlen, int 
     // Channel-parallel walking wins once there are enough channels to keep
     // the GPU busy.  With fewer, short sequences go to the time-parallel
     // CHUNKED variant and longer ones are cut into segments combined by the
-    // two-pass chunk carry (timed on GB300 over 64-4096 channels and 256-8192
-    // steps, bf16 and f32).
+    // two-pass chunk carry.  Boundaries timed on GB300 with 16 states, gate
+    // on, over 256-6144 channels and 512-32768 steps, for each I/O type (bf16
+    // rows are half the bytes, so the fused variant needs more channels
+    // before it wins).
     const int64_t nchan = (int64_t)batch * dim;
     if (nchan >= 4096) return SSM_VARIANT_FUSED;
-    if (seqlen <= 1024) return SSM_VARIANT_CHUNKED;
-    if (seqlen <= 2048 && nchan > 1024) return SSM_VARIANT_FUSED;
-    return SSM_VARIANT_TWOPASS;
+    const bool bf16 = io_dtype == SSM_BF16;
+    if (nchan >= 3072) return (bf16 && seqlen > 2048) ? SSM_VARIANT_TWOPASS : SSM_VARIANT_FUSED;
+    if (nchan >= 2048 && !bf16) return seqlen <= 2048 ? SSM_VARIANT_FUSED : SSM_VARIANT_TWOPASS;
+    return seqlen <= 2048 ? SSM_VARIANT_CHUNKED : SSM_VARIANT_TWOPASS;
 }
 
 size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype,

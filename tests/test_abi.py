@@ -9,6 +9,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import selective_state_space_02_gb300 as ssm
 from selective_state_space_02_gb300 import _native, build
@@ -66,7 +67,13 @@ def test_variant_selection_host_only(lib):
     assert ssm.select_variant(1, 64, 16, 1 << 20) == "twopass"
     assert ssm.select_variant(1, 64, 16, 256) == "chunked"
     assert ssm.select_variant(2, 1024, 16, 2048) == "fused"
-    assert ssm.select_variant(1, 512, 16, 2048) == "twopass"
+    assert ssm.select_variant(1, 512, 16, 2048) == "chunked"
+    assert ssm.select_variant(1, 512, 16, 4096) == "twopass"
+    # measured crossovers that depend on the I/O type
+    assert ssm.select_variant(1, 3072, 16, 8192) == "fused"
+    assert ssm.select_variant(1, 3072, 16, 8192, torch.bfloat16) == "twopass"
+    assert ssm.select_variant(1, 2048, 16, 1024) == "fused"
+    assert ssm.select_variant(1, 2048, 16, 1024, torch.bfloat16) == "chunked"
     assert lib.ssm_scan_select_variant(1, 1, 0, 10, 0) == ERR_DIMS
     assert lib.ssm_scan_select_variant(1, 1, 65, 10, 0) == ERR_DIMS
     assert lib.ssm_scan_select_variant(1, 1, 16, 10, 3) == ERR_DTYPE
