@@ -85,10 +85,13 @@ struct Shape {
     static constexpr int BR = NP + 1;               // padded B/C row (float2)
     // dB/dC term rows: channel stride CS and step stride TR (float2) chosen so
     // that a warp's term stores (CPW channels x LPC lanes) and the reduction's
-    // reads (8 steps x 4 states per warp) each take the minimum two wavefronts
+    // reads (8 steps x 4 states per warp) each take the minimum two wavefronts.
+    // A 64-bit access is served a half-warp at a time: the reduction's half-warp
+    // reads 8 steps x 2 states, which a step stride of 2 (mod 16 float2) spreads
+    // over all 16 bank pairs; a stride of 4 put steps j and j + 4 on one pair.
     static constexpr int CS = NP == 16 ? NP + 8 : NP;
-    static constexpr int TR = CPC * CS + 4;
-    static_assert(TR % 16 == 4, "term row stride");
+    static constexpr int TR = CPC * CS + 2;
+    static_assert(TR % 16 == 2, "term row stride");
     static constexpr int o_in = 0;                           // float4 [CPC][IR]: Delta, u, dq, x
     static constexpr int o_sz = o_in + 4 * IR * CPC;         // float2 [CPC][IR]: softplus'(v), dy silu'(z)
     static constexpr int o_bc = o_sz + 2 * IR * CPC;         // float2 [kChunk][BR]: B, C
