@@ -82,7 +82,8 @@ struct Shape {
     static constexpr int F = 8;                     // steps between reductions of the adjoint's terms
     // shared memory layout, in floats
     static constexpr int IR = kChunk + 1;           // padded per-channel row of the step inputs
-    static constexpr int BR = NP + 1;               // padded B/C row (float2)
+    static constexpr int BR = LPC + 1;              // padded row of B/C records (one per lane of a channel)
+    static constexpr int CR = NP + 1;               // padded C row of the adjoint totals pass
     // dB/dC term rows: channel stride CS and step stride TR (float2) chosen so
     // that a warp's term stores (CPW channels x LPC lanes) and the reduction's
     // reads (8 steps x 4 states per warp) each take the minimum two wavefronts.
@@ -94,21 +95,59 @@ struct Shape {
     static_assert(TR % 16 == 2, "term row stride");
     static constexpr int o_in = 0;                           // float4 [CPC][IR]: Delta, u, dq, x
     static constexpr int o_sz = o_in + 4 * IR * CPC;         // float2 [CPC][IR]: softplus'(v), dy silu'(z)
-    static constexpr int o_bc = o_sz + 2 * IR * CPC;         // float2 [kChunk][BR]: B, C
-    static constexpr int o_ta = o_bc + 2 * kChunk * BR;      // float4 [F][CPC][LPC]: per-lane sums over its states
+    static constexpr int o_bc = o_sz + 2 * IR * CPC;         // [kChunk][BR] records of 2 S2 floats: the B, then the C of a lane's states
+    static constexpr int o_ta = o_bc + 2 * S2 * kChunk * BR; // float4 [F][CPC][LPC]: per-lane sums over its states
     static constexpr int o_tb = o_ta + 4 * F * CPC * LPC;    // float2 [F][TR]: per-(channel, state) dB, dC terms
     static constexpr int o_bias = o_tb + 2 * F * TR;         // float [CPC]: dt_bias of the CTA's channels
     static constexpr size_t bytes = (size_t)(o_bias + CPC) * 4;
     // per-thread shares of the cooperative loops
     static constexpr int PER_T = CPC * kChunk / NT;           // (step, channel) items per thread
-    static constexpr int BC_T = kChunk * NP / NT;             // (step, state) items per thread
+    static constexpr int BC_T = kChunk * LPC / NT;            // (step, lane) B/C records per thread
     static constexpr int TA_T = (CPC * F + NT - 1) / NT;      // reduction over the states: (step, channel) items
     static constexpr int TB_T = (F * NP + NT - 1) / NT;       // reduction over the channels: (step, state) items
-    static_assert((CPC * kChunk) % NT == 0 && (kChunk * NP) % NT == 0 && NT % CPC == 0, "thread split");
+    static_assert((CPC * kChunk) % NT == 0 && (kChunk * LPC) % NT == 0 && NT % CPC == 0, "thread split");
+    static_assert(o_bc % 4 == 0 && o_ta % 4 == 0 && o_tb % 2 == 0, "16-byte records");
     static_assert(kChunk % SC == 0 && SC % F == 0 && LPC >= 8, "sub-chunks and term buffers");
 };
 
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + ex2(-v * kLog2e)); }
+
+// A lane's S2 states (li and li + LPC) as one value: a float, or a packed pair
+// whose arithmetic is one f32x2 instruction for both states.  Rec is the
+// lane's shared-memory record of one step: its states' B, then their C.
+template <int S2> struct Lane;
+template <> struct Lane<1> {
+    using V = float;
+    using Rec = float2;
+    static __device__ __forceinline__ V splat(float v) { return v; }
+    static __device__ __forceinline__ V make(const float (&v)[1]) { return v[0]; }
+    static __device__ __forceinline__ float at(V a, int) { return a; }
+    static __device__ __forceinline__ float sum(V a) { return a; }
+    static __device__ __forceinline__ V fma(V a, V b, V c) { return fmaf(a, b, c); }
+    static __device__ __forceinline__ V mul(V a, V b) { return a * b; }
+    static __device__ __forceinline__ V exp2(V a) { return ex2(a); }
+    static __device__ __forceinline__ Rec rec(const float (&b)[1], const float (&c)[1]) { return make_float2(b[0], c[0]); }
+    static __device__ __forceinline__ V B(Rec r) { return r.x; }
+    static __device__ __forceinline__ V C(Rec r) { return r.y; }
+    static __device__ __forceinline__ V load_B(const Rec *r) { return *reinterpret_cast<const float *>(r); }
+};
+template <> struct Lane<2> {
+    using V = float2;
+    using Rec = float4;
+    static __device__ __forceinline__ V splat(float v) { return make_float2(v, v); }
+    static __device__ __forceinline__ V make(const float (&v)[2]) { return make_float2(v[0], v[1]); }
+    static __device__ __forceinline__ float at(V a, int s) { return s ? a.y : a.x; }
+    static __device__ __forceinline__ float sum(V a) { return a.x + a.y; }
+    static __device__ __forceinline__ V fma(V a, V b, V c) { return __ffma2_rn(a, b, c); }
+    static __device__ __forceinline__ V mul(V a, V b) { return __fmul2_rn(a, b); }
+    static __device__ __forceinline__ V exp2(V a) { return make_float2(ex2(a.x), ex2(a.y)); }
+    static __device__ __forceinline__ Rec rec(const float (&b)[2], const float (&c)[2]) {
+        return make_float4(b[0], b[1], c[0], c[1]);
+    }
+    static __device__ __forceinline__ V B(Rec r) { return make_float2(r.x, r.y); }
+    static __device__ __forceinline__ V C(Rec r) { return make_float2(r.z, r.w); }
+    static __device__ __forceinline__ V load_B(const Rec *r) { return *reinterpret_cast<const float2 *>(r); }
+};
 
 // The raw inputs of one chunk, as each thread loads them (prefetched one
 // chunk ahead into registers) and unconverted: a float's bits, or a bf16 in
@@ -120,7 +159,7 @@ __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + ex2(
 template <int NP>
 struct Raw {
     uint32_t x[Shape<NP>::PER_T], v[Shape<NP>::PER_T], dy[Shape<NP>::PER_T], z[Shape<NP>::PER_T];
-    uint32_t B[Shape<NP>::BC_T], C[Shape<NP>::BC_T];
+    uint32_t B[Shape<NP>::BC_T * Shape<NP>::S2], C[Shape<NP>::BC_T * Shape<NP>::S2];   // [record][state of the lane]
 };
 
 template <typename T> __device__ __forceinline__ uint32_t ld_bits(const void *p, int64_t i);
@@ -152,11 +191,15 @@ __device__ __forceinline__ void load_raw(const BwdArgs &p, int b, int d0, int k,
     }
 #pragma unroll
     for (int i = 0; i < Sh::BC_T; ++i) {
-        const int e = threadIdx.x + i * Sh::NT;
-        const int n = e / kChunk, j = e % kChunk;
-        const int64_t idx = (n < p.N && j < jn) ? ((int64_t)b * p.N + n) * p.L + t0 + j : 0;
-        r.B[i] = ld_bits<T>(p.B, idx);
-        r.C[i] = ld_bits<T>(p.C, idx);
+        const int e = threadIdx.x + i * Sh::NT;          // = li * kChunk + j: a warp loads 32 steps of one row
+        const int li = e / kChunk, j = e % kChunk;
+#pragma unroll
+        for (int s = 0; s < Sh::S2; ++s) {
+            const int n = li + Sh::LPC * s;
+            const int64_t idx = (n < p.N && j < jn) ? ((int64_t)b * p.N + n) * p.L + t0 + j : 0;
+            r.B[i * Sh::S2 + s] = ld_bits<T>(p.B, idx);
+            r.C[i * Sh::S2 + s] = ld_bits<T>(p.C, idx);
+        }
     }
 }
 
@@ -183,7 +226,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
     constexpr int IR = Sh::IR, BR = Sh::BR, TR = Sh::TR;
     float4 *in = reinterpret_cast<float4 *>(sm + Sh::o_in);   // [CPC][IR]
     float2 *sz = reinterpret_cast<float2 *>(sm + Sh::o_sz);   // [CPC][IR]
-    float2 *bc = reinterpret_cast<float2 *>(sm + Sh::o_bc);   // [kChunk][BR]
+    using Ln = Lane<S2>;
+    using V = typename Ln::V;
+    using Rec = typename Ln::Rec;
+    Rec *bc = reinterpret_cast<Rec *>(sm + Sh::o_bc);         // [kChunk][BR]
     float4 *ta = reinterpret_cast<float4 *>(sm + Sh::o_ta);   // [F][CPC][LPC]
     float2 *tb = reinterpret_cast<float2 *>(sm + Sh::o_tb);   // [F][TR]
     float *sbias = sm + Sh::o_bias;                            // [CPC]
@@ -207,15 +253,20 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
     const int rj = tid % F, rc = tid / F, rd = d0 + rc;
     const float rD = (rthread && rd < dim && p.D) ? __ldg(p.D + rd) : 0.0f;
 
-    float Av[S2], A2[S2], lam[S2], dAacc[S2];
+    V Av, A2, lam, dAacc = Ln::splat(0.0f);
+    {
+        float av_[S2], a2_[S2], lam_[S2];
 #pragma unroll
-    for (int s = 0; s < S2; ++s) {
-        const int n = li + LPC * s;
-        const bool ok = dok && n < N;
-        Av[s] = ok ? __ldg(p.A + (int64_t)d * N + n) : 0.0f;
-        A2[s] = Av[s] * kLog2e;
-        lam[s] = (ok && p.lam_in) ? p.lam_in[((int64_t)blockIdx.z * nchan + chn) * N + n] : 0.0f;
-        dAacc[s] = 0.0f;
+        for (int s = 0; s < S2; ++s) {
+            const int n = li + LPC * s;
+            const bool ok = dok && n < N;
+            av_[s] = ok ? __ldg(p.A + (int64_t)d * N + n) : 0.0f;
+            a2_[s] = av_[s] * kLog2e;
+            lam_[s] = (ok && p.lam_in) ? p.lam_in[((int64_t)blockIdx.z * nchan + chn) * N + n] : 0.0f;
+        }
+        Av = Ln::make(av_);
+        A2 = Ln::make(a2_);
+        lam = Ln::make(lam_);
     }
     float sum_dD = 0.0f, sum_db = 0.0f;              // this thread's share of dD, ddt_bias (channel rc)
     if (tid < CPC) sbias[tid] = (p.dt_bias && d0 + tid < dim) ? __ldg(p.dt_bias + d0 + tid) : 0.0f;
@@ -255,14 +306,18 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
         }
 #pragma unroll
         for (int i = 0; i < Sh::BC_T; ++i) {
-            const int e = tid + i * NT;                     // = n * kChunk + j
-            const bool ok = e / kChunk < N && e % kChunk < jn;
-            bc[(e % kChunk) * BR + e / kChunk] =
-                ok ? make_float2(of_bits<T>(raw.B[i]), of_bits<T>(raw.C[i])) : make_float2(0.0f, 0.0f);
-        }
-        float hst[S2];                                      // the chunk's start state
+            const int e = tid + i * NT;                     // = lane-of-channel * kChunk + j
+            const int l = e / kChunk, j = e % kChunk;
+            float bv[S2], cv[S2];
 #pragma unroll
-        for (int s = 0; s < S2; ++s) hst[s] = hnext[s];
+            for (int s = 0; s < S2; ++s) {
+                const bool ok = l + LPC * s < N && j < jn;
+                bv[s] = ok ? of_bits<T>(raw.B[i * S2 + s]) : 0.0f;
+                cv[s] = ok ? of_bits<T>(raw.C[i * S2 + s]) : 0.0f;
+            }
+            bc[j * BR + l] = Ln::rec(bv, cv);
+        }
+        const V hst = Ln::make(hnext);                      // the chunk's start state
         __syncthreads();
         if (k > k_lo) {                                     // next chunk's inputs, in flight meanwhile
             load_raw<T, NP>(p, b, d0, k - 1, raw);
@@ -273,26 +328,22 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
         // the chunk's start again
         for (int sub = kChunk / SC - 1; sub >= 0; --sub) {
             const int j0 = sub * SC;
-            float h[S2][SC + 1];                            // h[s][j + 1] = state after step j0 + j
-            float av[S2][SC];                               // av[s][j] = a of step j0 + j (for the adjoint)
-#pragma unroll
-            for (int s = 0; s < S2; ++s) h[s][0] = hst[s];
+            const Rec *bcl = bc + li;                       // the lane's records, row stride BR
+            V h[SC + 1];                                    // h[j + 1] = state after step j0 + j
+            V av[SC];                                       // av[j] = a of step j0 + j (for the adjoint)
+            h[0] = hst;
 #pragma unroll 4
             for (int j = 0; j < j0; ++j) {
                 const float4 q = in[c * IR + j];
-#pragma unroll
-                for (int s = 0; s < S2; ++s)
-                    h[s][0] = fmaf(ex2(q.x * A2[s]), h[s][0], q.y * bc[j * BR + li + LPC * s].x);
+                h[0] = Ln::fma(Ln::exp2(Ln::mul(Ln::splat(q.x), A2)), h[0],
+                               Ln::mul(Ln::splat(q.y), Ln::load_B(bcl + j * BR)));
             }
             // ---- b. recompute the sub-chunk's states into registers ----------
 #pragma unroll
             for (int j = 0; j < SC; ++j) {
                 const float4 q = in[c * IR + j0 + j];
-#pragma unroll
-                for (int s = 0; s < S2; ++s) {
-                    av[s][j] = ex2(q.x * A2[s]);
-                    h[s][j + 1] = fmaf(av[s][j], h[s][j], q.y * bc[(j0 + j) * BR + li + LPC * s].x);
-                }
+                av[j] = Ln::exp2(Ln::mul(Ln::splat(q.x), A2));
+                h[j + 1] = Ln::fma(av[j], h[j], Ln::mul(Ln::splat(q.y), Ln::load_B(bcl + (j0 + j) * BR)));
             }
             // ---- c. the adjoint backwards, F steps between reductions ----------
 #pragma unroll
@@ -302,22 +353,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
                     const int jl = f * F + jj;                  // step within the sub-chunk
                     const int j = j0 + jl;
                     const float4 q = in[c * IR + j];
-                    float du = 0.0f, ds = 0.0f, pp = 0.0f;
+                    const Rec r = bcl[j * BR];
+                    const V Cv = Ln::C(r), a = av[jl], hn = h[jl + 1];
+                    lam = Ln::fma(Ln::splat(q.z), Cv, lam);
+                    const V daa = Ln::mul(Ln::mul(lam, h[jl]), a);  // (dL/da_t) a_t
+                    dAacc = Ln::fma(daa, Ln::splat(q.x), dAacc);
+                    const V du = Ln::mul(lam, Ln::B(r)), ds = Ln::mul(daa, Av), pp = Ln::mul(Cv, hn);
 #pragma unroll
-                    for (int s = 0; s < S2; ++s) {
-                        const int n = li + LPC * s;
-                        const float2 BC = bc[j * BR + n];
-                        lam[s] = fmaf(q.z, BC.y, lam[s]);
-                        const float a = av[s][jl];
-                        const float daa = lam[s] * h[s][jl] * a;     // (dL/da_t) a_t
-                        dAacc[s] = fmaf(daa, q.x, dAacc[s]);
-                        du = fmaf(lam[s], BC.x, du);
-                        ds = fmaf(daa, Av[s], ds);
-                        pp = fmaf(BC.y, h[s][jl + 1], pp);
-                        tb[jj * TR + c * Sh::CS + n] = make_float2(lam[s] * q.y, q.z * h[s][jl + 1]);
-                        lam[s] *= a;
-                    }
-                    ta[(jj * CPC + c) * LPC + li] = make_float4(du, ds, pp, 0.0f);
+                    for (int s = 0; s < S2; ++s)
+                        tb[jj * TR + c * Sh::CS + li + LPC * s] = make_float2(Ln::at(lam, s) * q.y, q.z * Ln::at(hn, s));
+                    // the lane's sums over its states (the two C h terms summed by the reduction)
+                    ta[(jj * CPC + c) * LPC + li] =
+                        make_float4(Ln::sum(du), Ln::sum(ds), Ln::at(pp, 0), S2 == 2 ? Ln::at(pp, S2 - 1) : 0.0f);
+                    lam = Ln::mul(lam, a);
                 }
                 __syncthreads();
                 // sums over each channel's lanes: dx, ddelta, dz of (step, channel)
@@ -331,7 +379,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
                         const float4 t = row[(m + rot) & (LPC - 1)];
                         du += t.x;
                         ds += t.y;
-                        pp += t.z;
+                        pp += t.z + t.w;
                     }
                     if (rd < dim && j < jn) {
                         const float4 q = in[rc * IR + j];
@@ -372,8 +420,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
     for (int s = 0; s < S2; ++s) {
         const int n = li + LPC * s;
         if (dok && n < N) {
-            atomicAdd(p.dA + (int64_t)d * N + n, dAacc[s]);
-            if (p.dh0 && blockIdx.z == 0) p.dh0[chn * N + n] = lam[s];   // the adjoint of the start state
+            atomicAdd(p.dA + (int64_t)d * N + n, Ln::at(dAacc, s));
+            if (p.dh0 && blockIdx.z == 0) p.dh0[chn * N + n] = Ln::at(lam, s);   // the adjoint of the start state
         }
     }
     if (rthread && rd < dim) {
@@ -390,11 +438,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
 template <typename T, int NP>
 __global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArgs p, float *q_out, float *s_out) {
     using Sh = Shape<NP>;
-    constexpr int LPC = Sh::LPC, S2 = Sh::S2, CPW = Sh::CPW, CPC = Sh::CPC, NT = Sh::NT, IR = Sh::IR, BR = Sh::BR;
+    constexpr int LPC = Sh::LPC, S2 = Sh::S2, CPW = Sh::CPW, CPC = Sh::CPC, NT = Sh::NT, IR = Sh::IR, CR = Sh::CR;
     extern __shared__ __align__(16) float sm[];
     float2 *dd = reinterpret_cast<float2 *>(sm);            // [CPC][IR]: Delta, dq
-    float *cs = sm + 2 * CPC * IR;                          // [kChunk][BR]: C
-    float *sbias = cs + kChunk * BR;                        // [CPC]: dt_bias of the CTA's channels
+    float *cs = sm + 2 * CPC * IR;                          // [kChunk][CR]: C
+    float *sbias = cs + kChunk * CR;                        // [CPC]: dt_bias of the CTA's channels
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int li = lane % LPC;
@@ -441,9 +489,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArg
         }
 #pragma unroll
         for (int i = 0; i < Sh::BC_T; ++i) {
-            const int e = tid + i * NT;                     // = n * kChunk + j
-            const bool ok = e / kChunk < N && e % kChunk < jn;
-            cs[(e % kChunk) * BR + e / kChunk] = ok ? of_bits<T>(raw.C[i]) : 0.0f;
+            const int e = tid + i * NT;                     // = lane-of-channel * kChunk + j
+            const int l = e / kChunk, j = e % kChunk;
+#pragma unroll
+            for (int s = 0; s < S2; ++s) {
+                const int n = l + LPC * s;
+                cs[j * CR + n] = (n < N && j < jn) ? of_bits<T>(raw.C[i * S2 + s]) : 0.0f;
+            }
         }
         __syncthreads();
         if (k > k_lo) load_raw<T, NP>(p, b, d0, k - 1, raw);
@@ -452,7 +504,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) adj_totals_kernel(const BwdArg
             const float2 q = dd[c * IR + j];
 #pragma unroll
             for (int s = 0; s < S2; ++s)
-                lam[s] = fmaf(q.y, cs[j * BR + li + LPC * s], lam[s]) * ex2(q.x * A2[s]);
+                lam[s] = fmaf(q.y, cs[j * CR + li + LPC * s], lam[s]) * ex2(q.x * A2[s]);
             ssum += q.x;
         }
         __syncthreads();
@@ -537,7 +589,7 @@ cudaError_t launch_np(BwdArgs a, const Plan &pl, const float *dfinal, char *seg_
         const int64_t nchan = (int64_t)a.batch * a.dim;
         float *q = reinterpret_cast<float *>(seg_ws);
         float *ssum = reinterpret_cast<float *>(seg_ws + r256((size_t)pl.nseg * nchan * a.N * 4));
-        const size_t tb = (size_t)(2 * Sh::CPC * Sh::IR + kChunk * Sh::BR + Sh::CPC) * 4;
+        const size_t tb = (size_t)(2 * Sh::CPC * Sh::IR + kChunk * Sh::CR + Sh::CPC) * 4;
         adj_totals_kernel<T, NP><<<dim3(gx, (unsigned)a.batch, (unsigned)pl.nseg), kWarps * 32, tb, st>>>(a, q, ssum);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         const int64_t pairs = nchan * a.N;
