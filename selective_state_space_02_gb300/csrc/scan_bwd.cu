@@ -106,7 +106,7 @@ struct Shape {
     static constexpr int TA_T = (CPC * F + NT - 1) / NT;      // reduction over the states: (step, channel) items
     static constexpr int TB_T = (F * NP + NT - 1) / NT;       // reduction over the channels: (step, state) items
     static_assert((CPC * kChunk) % NT == 0 && (kChunk * LPC) % NT == 0 && NT % CPC == 0, "thread split");
-    static_assert(o_bc % 4 == 0 && o_ta % 4 == 0 && o_tb % 2 == 0, "16-byte records");
+    static_assert(o_bc % 4 == 0 && o_ta % 4 == 0 && o_tb % 2 == 0 && CPC % 2 == 0, "16-byte records, channel pairs");
     static_assert(kChunk % SC == 0 && SC % F == 0 && LPC >= 8, "sub-chunks and term buffers");
 };
 
@@ -373,14 +373,14 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
                     const int j = j0 + f * F + rj;
                     const float4 *row = ta + (rj * CPC + rc) * LPC;
                     const int rot = tid & 7;                     // 8 lanes, 8 bank groups
-                    float du = 0.0f, ds = 0.0f, pp = 0.0f;
+                    float2 s01 = make_float2(0.0f, 0.0f), s23 = make_float2(0.0f, 0.0f);
 #pragma unroll
                     for (int m = 0; m < LPC; ++m) {
                         const float4 t = row[(m + rot) & (LPC - 1)];
-                        du += t.x;
-                        ds += t.y;
-                        pp += t.z + t.w;
+                        s01 = __fadd2_rn(s01, make_float2(t.x, t.y));
+                        s23 = __fadd2_rn(s23, make_float2(t.z, t.w));
                     }
+                    const float du = s01.x, ds = s01.y, pp = s23.x + s23.y;
                     if (rd < dim && j < jn) {
                         const float4 q = in[rc * IR + j];
                         const float2 g = sz[rc * IR + j];
@@ -400,16 +400,17 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
                     const int jj = e % F, n = e / F;
                     const int j = j0 + f * F + jj;
                     if (e < F * NP && n < N && j < jn) {
-                        float db = 0.0f, dc = 0.0f;
+                        // (dB, dC) pairs summed packed, two chains over the channels
+                        float2 s0 = make_float2(0.0f, 0.0f), s1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-                        for (int cc = 0; cc < CPC; ++cc) {
-                            const float2 t = tb[jj * TR + cc * Sh::CS + n];
-                            db += t.x;
-                            dc += t.y;
+                        for (int cc = 0; cc < CPC; cc += 2) {
+                            s0 = __fadd2_rn(s0, tb[jj * TR + cc * Sh::CS + n]);
+                            s1 = __fadd2_rn(s1, tb[jj * TR + (cc + 1) * Sh::CS + n]);
                         }
+                        const float2 g = __fadd2_rn(s0, s1);
                         const int64_t idx = ((int64_t)b * N + n) * L + t0 + j;
-                        atomicAdd(p.dB + idx, db);
-                        atomicAdd(p.dC + idx, dc);
+                        atomicAdd(p.dB + idx, g.x);
+                        atomicAdd(p.dC + idx, g.y);
                     }
                 }
                 __syncthreads();   // the term buffers are refilled by the next group
