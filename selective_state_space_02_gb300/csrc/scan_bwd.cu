@@ -22,13 +22,15 @@
 //         (the last SC steps first; a sub-chunk's start state is advanced from
 //         the chunk's start again);
 //      c. (serial, per lane) the state's adjoint backwards over those steps,
-//         lambda <- lambda + dq C, then lambda <- a lambda, writing per step
-//         the lane's terms (lambda B, lambda h_{t-1} a A and C h summed over
-//         its states; lambda u and dq h per state) to shared memory;
-//      d. (parallel, every F steps) per (step, channel), the sums over the
-//         lanes' terms finish dx, ddelta and dz; per (step, state), dB and dC
-//         summed over the CTA's channels are added to global memory (one
-//         atomic addition per element per CTA); dA accumulates per lane;
+//         lambda <- lambda + dq C, then lambda <- a lambda, with per step the
+//         lane's terms lambda B, lambda h_{t-1} a A and C h summed over its
+//         states (reduce-scattered over the channel's lanes by shuffles, so
+//         that after F steps each of F lanes holds one step's sums and
+//         finishes its dx, ddelta and dz), and lambda u and dq h per state
+//         written to shared memory;
+//      d. (parallel, every F steps) per (step, state), dB and dC summed over
+//         the CTA's channels are added to global memory (one atomic addition
+//         per element per CTA); dA accumulates per lane;
 //    and at the end adds dA, dD and ddt_bias (shared by batches) and writes
 //    the start state's gradient.
 #include "../../include/ssm_bwd.h"
@@ -96,21 +98,30 @@ struct Shape {
     static constexpr int o_in = 0;                           // float4 [CPC][IR]: Delta, u, dq, x
     static constexpr int o_sz = o_in + 4 * IR * CPC;         // float2 [CPC][IR]: softplus'(v), dy silu'(z)
     static constexpr int o_bc = o_sz + 2 * IR * CPC;         // [kChunk][BR] records of 2 S2 floats: the B, then the C of a lane's states
-    static constexpr int o_ta = o_bc + 2 * S2 * kChunk * BR; // float4 [F][CPC][LPC]: per-lane sums over its states
-    static constexpr int o_tb = o_ta + 4 * F * CPC * LPC;    // float2 [F][TR]: per-(channel, state) dB, dC terms
+    static constexpr int o_tb = o_bc + 2 * S2 * kChunk * BR; // float2 [F][TR]: per-(channel, state) dB, dC terms
     static constexpr int o_bias = o_tb + 2 * F * TR;         // float [CPC]: dt_bias of the CTA's channels
     static constexpr size_t bytes = (size_t)(o_bias + CPC) * 4;
     // per-thread shares of the cooperative loops
     static constexpr int PER_T = CPC * kChunk / NT;           // (step, channel) items per thread
     static constexpr int BC_T = kChunk * LPC / NT;            // (step, lane) B/C records per thread
-    static constexpr int TA_T = (CPC * F + NT - 1) / NT;      // reduction over the states: (step, channel) items
     static constexpr int TB_T = (F * NP + NT - 1) / NT;       // reduction over the channels: (step, state) items
     static_assert((CPC * kChunk) % NT == 0 && (kChunk * LPC) % NT == 0 && NT % CPC == 0, "thread split");
-    static_assert(o_bc % 4 == 0 && o_ta % 4 == 0 && o_tb % 2 == 0 && CPC % 2 == 0, "16-byte records, channel pairs");
-    static_assert(kChunk % SC == 0 && SC % F == 0 && LPC >= 8, "sub-chunks and term buffers");
+    static_assert(o_bc % 4 == 0 && o_tb % 2 == 0 && CPC % 2 == 0, "16-byte records, channel pairs");
+    static_assert(kChunk % SC == 0 && SC % F == 0 && F == 8 && LPC >= F, "sub-chunks; F steps over a channel's lanes");
 };
 
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + ex2(-v * kLog2e)); }
+
+// One round of a reduce-scatter over the lane pairs (lane, lane ^ m): of the
+// two triples a lane holds it keeps the one its bit m selects (hi where set)
+// and adds its partner's copy of that one.
+__device__ __forceinline__ float3 rs_round(const float3 &hi, const float3 &lo, int m) {
+    const bool up = (threadIdx.x & m) != 0;
+    const float3 keep = up ? hi : lo, send = up ? lo : hi;
+    return make_float3(keep.x + __shfl_xor_sync(0xffffffffu, send.x, m),
+                       keep.y + __shfl_xor_sync(0xffffffffu, send.y, m),
+                       keep.z + __shfl_xor_sync(0xffffffffu, send.z, m));
+}
 
 // A lane's S2 states (li and li + LPC) as one value: a float, or a packed pair
 // whose arithmetic is one f32x2 instruction for both states.  Rec is the
@@ -230,7 +241,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
     using V = typename Ln::V;
     using Rec = typename Ln::Rec;
     Rec *bc = reinterpret_cast<Rec *>(sm + Sh::o_bc);         // [kChunk][BR]
-    float4 *ta = reinterpret_cast<float4 *>(sm + Sh::o_ta);   // [F][CPC][LPC]
     float2 *tb = reinterpret_cast<float2 *>(sm + Sh::o_tb);   // [F][TR]
     float *sbias = sm + Sh::o_bias;                            // [CPC]
     const int tid = threadIdx.x;
@@ -247,11 +257,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
     const int64_t chn = (int64_t)b * dim + d;
     const bool has_z = p.z != nullptr;
     const int nchunk = (int)((L + kChunk - 1) / kChunk);
-    // the (step, channel) reduction threads: step rj of each group of F steps
-    // (consecutive threads: consecutive steps), channel rc
-    const bool rthread = tid < CPC * F;
-    const int rj = tid % F, rc = tid / F, rd = d0 + rc;
-    const float rD = (rthread && rd < dim && p.D) ? __ldg(p.D + rd) : 0.0f;
+    const float Dd = (dok && p.D) ? __ldg(p.D + d) : 0.0f;
 
     V Av, A2, lam, dAacc = Ln::splat(0.0f);
     {
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
         A2 = Ln::make(a2_);
         lam = Ln::make(lam_);
     }
-    float sum_dD = 0.0f, sum_db = 0.0f;              // this thread's share of dD, ddt_bias (channel rc)
+    float sum_dD = 0.0f, sum_db = 0.0f;              // this lane's share of dD, ddt_bias (its channel)
     if (tid < CPC) sbias[tid] = (p.dt_bias && d0 + tid < dim) ? __ldg(p.dt_bias + d0 + tid) : 0.0f;
     __syncthreads();
 
@@ -348,6 +354,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
             // ---- c. the adjoint backwards, F steps between reductions ----------
 #pragma unroll
             for (int f = SC / F - 1; f >= 0; --f) {
+                // the lane's sums over its states (du, ds, pp) of the F steps,
+                // reduce-scattered over the channel's lanes as they come: pairs
+                // of steps over lane bit 0, pairs of pairs over bit 1, the two
+                // halves over bit 2, so lane li ends with step li's sums over
+                // 8 lanes
+                float3 tv[F], wa[F / 2], wb[F / 4];
 #pragma unroll
                 for (int jj = F - 1; jj >= 0; --jj) {
                     const int jl = f * F + jj;                  // step within the sub-chunk
@@ -362,37 +374,34 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
 #pragma unroll
                     for (int s = 0; s < S2; ++s)
                         tb[jj * TR + c * Sh::CS + li + LPC * s] = make_float2(Ln::at(lam, s) * q.y, q.z * Ln::at(hn, s));
-                    // the lane's sums over its states (the two C h terms summed by the reduction)
-                    ta[(jj * CPC + c) * LPC + li] =
-                        make_float4(Ln::sum(du), Ln::sum(ds), Ln::at(pp, 0), S2 == 2 ? Ln::at(pp, S2 - 1) : 0.0f);
+                    tv[jj] = make_float3(Ln::sum(du), Ln::sum(ds), Ln::sum(pp));
+                    if (jj % 2 == 0) wa[jj / 2] = rs_round(tv[jj + 1], tv[jj], 1);
+                    if (jj % 4 == 0) wb[jj / 4] = rs_round(wa[jj / 2 + 1], wa[jj / 2], 2);
                     lam = Ln::mul(lam, a);
                 }
-                __syncthreads();
-                // sums over each channel's lanes: dx, ddelta, dz of (step, channel)
-                if (rthread) {
-                    const int j = j0 + f * F + rj;
-                    const float4 *row = ta + (rj * CPC + rc) * LPC;
-                    const int rot = tid & 7;                     // 8 lanes, 8 bank groups
-                    float2 s01 = make_float2(0.0f, 0.0f), s23 = make_float2(0.0f, 0.0f);
+                float3 w = rs_round(wb[1], wb[0], 4);
 #pragma unroll
-                    for (int m = 0; m < LPC; ++m) {
-                        const float4 t = row[(m + rot) & (LPC - 1)];
-                        s01 = __fadd2_rn(s01, make_float2(t.x, t.y));
-                        s23 = __fadd2_rn(s23, make_float2(t.z, t.w));
-                    }
-                    const float du = s01.x, ds = s01.y, pp = s23.x + s23.y;
-                    if (rd < dim && j < jn) {
-                        const float4 q = in[rc * IR + j];
-                        const float2 g = sz[rc * IR + j];
-                        const float dv = fmaf(du, q.w, ds) * g.x;
-                        const int64_t idx = ((int64_t)b * dim + rd) * L + t0 + j;
-                        Io<T>::st(p.dx, idx, fmaf(du, q.x, q.z * rD));
+                for (int m = F; m < LPC; m <<= 1) {         // wider channels: the 8-lane groups' sums added
+                    w.x += __shfl_xor_sync(0xffffffffu, w.x, m);
+                    w.y += __shfl_xor_sync(0xffffffffu, w.y, m);
+                    w.z += __shfl_xor_sync(0xffffffffu, w.z, m);
+                }
+                // dx, ddelta, dz of the lane's step (one lane per step and channel)
+                {
+                    const int j = j0 + f * F + (li & (F - 1));
+                    if (li < F && dok && j < jn) {
+                        const float4 q = in[c * IR + j];
+                        const float2 g = sz[c * IR + j];
+                        const float dv = fmaf(w.x, q.w, w.y) * g.x;
+                        const int64_t idx = chn * L + t0 + j;
+                        Io<T>::st(p.dx, idx, fmaf(w.x, q.x, q.z * Dd));
                         Io<T>::st(p.ddelta, idx, dv);
-                        if (has_z) Io<T>::st(p.dz, idx, g.y * fmaf(rD, q.w, pp));
+                        if (has_z) Io<T>::st(p.dz, idx, g.y * fmaf(Dd, q.w, w.z));
                         sum_dD = fmaf(q.z, q.w, sum_dD);
                         sum_db += dv;
                     }
                 }
+                __syncthreads();
                 // sums over the CTA's channels: dB, dC of (step, state)
 #pragma unroll
                 for (int i = 0; i < Sh::TB_T; ++i) {
@@ -425,9 +434,14 @@ __global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
             if (p.dh0 && blockIdx.z == 0) p.dh0[chn * N + n] = Ln::at(lam, s);   // the adjoint of the start state
         }
     }
-    if (rthread && rd < dim) {
-        if (p.dD) atomicAdd(p.dD + rd, sum_dD);
-        if (p.ddt_bias) atomicAdd(p.ddt_bias + rd, sum_db);
+#pragma unroll
+    for (int m = 1; m < LPC; m <<= 1) {
+        sum_dD += __shfl_xor_sync(0xffffffffu, sum_dD, m);
+        sum_db += __shfl_xor_sync(0xffffffffu, sum_db, m);
+    }
+    if (dok && li == 0) {
+        if (p.dD) atomicAdd(p.dD + d, sum_dD);
+        if (p.ddt_bias) atomicAdd(p.ddt_bias + d, sum_db);
     }
 }
 
