@@ -227,10 +227,10 @@ __device__ __forceinline__ void load_start(const BwdArgs &p, int k, int64_t chn,
     }
 }
 
-template <typename T, int NP>
-// Three CTAs per SM (at most 168 registers): the walk is latency-bound, and the
-// extra CTA outweighs the few spilled bytes (mid 1.03 -> 0.87 ms, wide 29.4 -> 23.2 ms).
-__global__ void __launch_bounds__(kWarps * 32, 3) bwd_kernel(const BwdArgs p) {
+// MINB CTAs per SM: 3 (at most 168 registers, no spills) or 4 (at most 128,
+// a few spilled bytes); the launch picks by grid size (launch_np).
+template <typename T, int NP, int MINB>
+__global__ void __launch_bounds__(kWarps * 32, MINB) bwd_kernel(const BwdArgs p) {
     using Sh = Shape<NP>;
     constexpr int LPC = Sh::LPC, S2 = Sh::S2, CPW = Sh::CPW, CPC = Sh::CPC, NT = Sh::NT, F = Sh::F, SC = Sh::SC;
     extern __shared__ __align__(16) float sm[];
@@ -613,7 +613,13 @@ cudaError_t launch_np(BwdArgs a, const Plan &pl, const float *dfinal, char *seg_
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         a.lam_in = q;
     }
-    auto kern = bwd_kernel<T, NP>;
+    // The walk is latency-bound: a grid that fits one wave of 3 CTAs per SM
+    // runs them without spills (mid, 384 CTAs, 2.5 per SM either way: 0.523
+    // against 0.539 ms with 4); larger grids take 4 CTAs per SM, whose extra
+    // warps outweigh the spilled bytes and whose waves are fewer (large
+    // 2.42 -> 2.19 ms, wide 12.41 -> 12.19 ms).
+    const int64_t ctas = (int64_t)gx * a.batch * pl.nseg;
+    auto kern = ctas > kWaveCtas ? bwd_kernel<T, NP, 4> : bwd_kernel<T, NP, 3>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::bytes);
     if (e != cudaSuccess) return e;
     kern<<<dim3(gx, (unsigned)a.batch, (unsigned)pl.nseg), kWarps * 32, Sh::bytes, st>>>(a);

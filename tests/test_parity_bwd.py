@@ -100,6 +100,9 @@ def _compare(g, ref, dtype):
     ((2, 2440, 13, 70), "bf16", False),   # rows not 16-byte aligned (element loads), padded states
     ((1, 5120, 64, 40), "bf16", True),    # 64 states: 16-step tiles, a state every other tile
     ((1, 2440, 16, 96), "f32", True),     # the pass at 2 states a lane; walk split into segments
+    # more CTAs than one wave of 3 per SM: the walk at 4 CTAs per SM
+    ((2, 4000, 16, 40), "f32", True),
+    ((2, 4000, 16, 75), "bf16", False),
 ])
 def test_backward_matches_oracle(shape, dtype, gate):
     p = synth.make_problem(*shape, dtype=dtype, gate=gate, seed=400 + shape[2] + shape[3], A_mode="random")
@@ -150,20 +153,22 @@ def test_empty_sequence():
     assert float(g["dA"].abs().max()) == 0.0 and float(g["dD"].abs().max()) == 0.0
 
 
-def test_large_workload_sampled():
-    """The mid-size shape (4 x 1536 x 16, 2048 steps, bf16), in the launch
-    configuration it gets at that size: the per-channel gradients (dx, ddelta,
-    dz) of sampled channels against the oracle run on those channels alone.
-    (dA, dB, dC, dD and ddt_bias are sums over all channels or batches; the
-    smaller cases above check them.)"""
-    p = synth.make_problem(4, 1536, 16, 2048, dtype="bf16", gate=True, seed=428)
+@pytest.mark.parametrize("shape", [(4, 1536, 16, 2048), (8, 2048, 16, 4096)], ids=["mid", "large"])
+def test_large_workload_sampled(shape):
+    """The mid-size (4 x 1536 x 16, 2048 steps) and large-batch (8 x 2048 x 16,
+    4096 steps) bf16 shapes, in the launch configurations they get at those
+    sizes (the walk at 3 and at 4 CTAs per SM): the per-channel gradients (dx,
+    ddelta, dz) of sampled channels against the oracle run on those channels
+    alone.  (dA, dB, dC, dD and ddt_bias are sums over all channels or
+    batches; the smaller cases above check them.)"""
+    p = synth.make_problem(*shape, dtype="bf16", gate=True, seed=428)
     dy = _dy(p, 10)
     dev = lambda t: None if t is None else t.cuda()
     g = ssm.scan_bwd(dev(p.x), dev(p.delta), dev(p.A), dev(p.B), dev(p.C), dev(dy), D=dev(p.D), z=dev(p.z),
                      dt_bias=dev(p.dt_bias))
     torch.cuda.synchronize()
     rng = np.random.default_rng(0)
-    for b, d in [(int(rng.integers(4)), int(rng.integers(1536))) for _ in range(6)]:
+    for b, d in [(int(rng.integers(p.batch)), int(rng.integers(p.dim))) for _ in range(6)]:
         sl = lambda t: None if t is None else t[b:b + 1, d:d + 1].contiguous()
         ref = oracle.bwd(sl(p.x).float().numpy(), sl(p.delta).float().numpy(), p.A[d:d + 1].numpy(),
                          p.B[b:b + 1].float().numpy(), p.C[b:b + 1].float().numpy(), sl(dy).float().numpy(),
