@@ -763,6 +763,36 @@ def run_bwd(args):
                "h2d_bytes_per_step": sum(v[0].numel() * v[0].element_size() for v in hin.values()),
                "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in outs.values()),
                "api": "scan_bwd with its inputs copied from pinned host memory and the gradients copied back"}
+    # The training pair, timed after the line's own region: a forward that
+    # stores the chunk-start states with the backward from them
+    # (ssm_scan_fwd_ckpt + ssm_scan_bwd_ckpt), against the forward followed by
+    # the backward that computes them again; L2 flushed before each pair.
+    lib = ssm._native.load()
+    code = ssm._dtype_code(p.torch_dtype)
+    sizes = (p.batch, p.dim, p.dstate, p.seqlen, code)
+    u8 = lambda n: torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+    fws, fwc, bwc = (u8(lib.ssm_scan_fwd_workspace_size(*sizes, 0)), u8(lib.ssm_scan_fwd_ckpt_workspace_size(*sizes, 0)),
+                     u8(lib.ssm_scan_bwd_ckpt_workspace_size(*sizes)))
+    fkw = dict(D=D, z=z, dt_bias=bias, delta_softplus=p.delta_softplus, y=torch.empty_like(x))
+    bkw = dict(D=D, z=z, dt_bias=bias, delta_softplus=p.delta_softplus, workspace=bwc)
+
+    def pair_plain():
+        ssm.scan_fwd(x, dl, A, B, C, workspace=fws, **fkw)
+        step()
+
+    def pair_ckpt():
+        _, ck = ssm.scan_fwd(x, dl, A, B, C, workspace=fwc, return_ckpt=True, **fkw)
+        ssm.scan_bwd(x, dl, A, B, C, ddy, ckpt=ck, **bkw)
+
+    _, ck0 = ssm.scan_fwd(x, dl, A, B, C, workspace=fwc, return_ckpt=True, **fkw)
+    t_plain = statistics.mean(_timed_steps(pair_plain, args, flush, stream, world))
+    t_ckpt = statistics.mean(_timed_steps(pair_ckpt, args, flush, stream, world))
+    t_bwd_ckpt = statistics.mean(_timed_steps(lambda: ssm.scan_bwd(x, dl, A, B, C, ddy, ckpt=ck0, **bkw),
+                                              args, flush, stream, world))
+    training = {"fwd_then_bwd_ms": round(t_plain, 5), "fwd_ckpt_then_bwd_ckpt_ms": round(t_ckpt, 5),
+                "bwd_from_ckpt_ms": round(t_bwd_ckpt, 5),
+                "note": "ms per pair (CUDA events, rank 0); the forward with checkpoints stores the state at every "
+                        "32-step chunk start and the backward from them skips its chunk-start states pass"}
     line = {
         "metric": BWD_METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
@@ -774,6 +804,7 @@ def run_bwd(args):
         "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
         "gpu_launches": args.steps * bwd_kernels,
+        "training_step": training,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -87,6 +87,32 @@ int ssm_scan_bwd(const void *x, const void *delta, const float *A, const void *B
                  int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                  void *workspace, size_t workspace_bytes, void *stream);
 
+/* Device workspace, in bytes, of ssm_scan_bwd_ckpt (segment sums of walks
+ * split into segments; often 0); (size_t)-1 for invalid sizes. */
+size_t ssm_scan_bwd_ckpt_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype);
+
+/* Kernels one ssm_scan_bwd_ckpt call launches: the reverse walk, plus the
+ * adjoint totals and their carry for walks split into segments.  0 for an
+ * empty problem, -1 for invalid sizes.  Host only. */
+int ssm_scan_bwd_ckpt_kernel_count(int batch, int dim, int dstate, int64_t seqlen);
+
+/*
+ * The backward from the checkpoints a forward wrote (ssm_scan_fwd_ckpt,
+ * ssm_scan.h): ssm_scan_bwd without the chunk-start states pass.
+ *   ckpt          required input.  The checkpoints of ssm_scan_fwd_ckpt over
+ *                 the same inputs and start state, ssm_scan_ckpt_size() bytes;
+ *                 the start state enters only through them.
+ * Every other argument as ssm_scan_bwd (which takes initial_state where this
+ * takes ckpt); the workspace is ssm_scan_bwd_ckpt_workspace_size() bytes.
+ */
+int ssm_scan_bwd_ckpt(const void *x, const void *delta, const float *A, const void *B, const void *C,
+                      const float *D, const void *z, const float *dt_bias, int delta_softplus,
+                      const float *ckpt, const void *dy, const float *dfinal_state,
+                      void *dx, void *ddelta, float *dA, float *dB, float *dC, float *dD, void *dz,
+                      float *ddt_bias, float *dinitial_state,
+                      int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -174,6 +174,38 @@ int ssm_scan_fwd_from_state(const void *x, const void *delta, const float *A, co
                             int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                             void *workspace, size_t workspace_bytes, void *stream, int variant);
 
+/* Bytes of the checkpoints of ssm_scan_fwd_ckpt: ceil(seqlen / 32) chunk
+ * states of [batch, dim, dstate] float32.  (size_t)-1 for invalid sizes. */
+size_t ssm_scan_ckpt_size(int batch, int dim, int dstate, int64_t seqlen);
+
+/* Device workspace, in bytes, of ssm_scan_fwd_ckpt for `variant`; (size_t)-1
+ * for invalid sizes or a variant that cannot write checkpoints. */
+size_t ssm_scan_fwd_ckpt_workspace_size(int batch, int dim, int dstate, int64_t seqlen,
+                                        int io_dtype, int variant);
+
+/*
+ * Forward for training: ssm_scan_fwd_from_state that also stores the state
+ * at the start of every 32-step chunk, the boundary states the backward
+ * recomputes each chunk from ("Mamba (part 2)" sect. 4.3: store the states
+ * at chunk boundaries, recompute inside the chunk).  ssm_scan_bwd_ckpt
+ * (ssm_bwd.h) then starts from them instead of computing them again.
+ *   ckpt          required output.  [ceil(seqlen / 32)][batch * dim][dstate]
+ *                 float32, 4-byte aligned, ssm_scan_ckpt_size() bytes; entry
+ *                 k is h before step 32 k (entry 0: initial_state, or 0).  It
+ *                 must not overlap any input or output.
+ *   variant       FUSED or TWOPASS store the checkpoints as they go; AUTO
+ *                 resolves as for ssm_scan_fwd but takes TWOPASS where that
+ *                 would pick CHUNKED; CHUNKED returns SSM_ERR_UNSUPPORTED.
+ *   workspace     at least ssm_scan_fwd_ckpt_workspace_size() bytes.
+ * y and final_state are those of ssm_scan_fwd_from_state with the same
+ * variant (the same kernels, with the extra stores).
+ */
+int ssm_scan_fwd_ckpt(const void *x, const void *delta, const float *A, const void *B,
+                      const void *C, const float *D, const void *z, const float *dt_bias,
+                      int delta_softplus, const float *initial_state, void *y, float *final_state,
+                      float *ckpt, int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                      void *workspace, size_t workspace_bytes, void *stream, int variant);
+
 /* Device status of earlier launches on the current device: bit 0 is set when
  * a kernel's bounded wait on its own TMA copies gave up (the output of that
  * call is then invalid).  Synchronises `stream`; `clear` nonzero resets the

@@ -99,7 +99,7 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
              dt_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
              return_final_state: bool = False, variant="auto", y: Optional[torch.Tensor] = None,
              final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-             initial_state: Optional[torch.Tensor] = None):
+             initial_state: Optional[torch.Tensor] = None, return_ckpt: bool = False):
     """Forward selective scan on CUDA tensors, launched on the current stream.
 
     x, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (float32 or
@@ -109,7 +109,10 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
     ``workspace`` may be given to avoid allocations.  ``initial_state``
     [batch, dim, dstate] float32 starts the recurrence from that state (a
     resumed segment); ``final_state`` may be the same tensor to advance it in
-    place.
+    place.  With ``return_ckpt`` the forward also stores the state at the
+    start of every 32-step chunk (ssm_scan_fwd_ckpt), returned last as a
+    float32 [ceil(L / 32), batch, dim, dstate] tensor for ``scan_bwd(...,
+    ckpt=...)``.
     """
     batch, dim, N, L = _check_inputs(x, delta, A, B, C, D, z, dt_bias, "cuda")
     if initial_state is not None:
@@ -126,14 +129,22 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
         y = torch.empty_like(x)
     if return_final_state and final_state is None:
         final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=x.device)
-    ws_bytes = lib.ssm_scan_fwd_workspace_size(batch, dim, N, L, code, v)
+    ws_bytes = (lib.ssm_scan_fwd_ckpt_workspace_size if return_ckpt else lib.ssm_scan_fwd_workspace_size)(
+        batch, dim, N, L, code, v)
     if ws_bytes == (1 << 64) - 1:
-        raise ScanError(-2, "invalid sizes")
+        raise ScanError(-2, "invalid sizes or a variant without checkpoints")
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
     stream = torch.cuda.current_stream(x.device).cuda_stream
     fs = _ptr(final_state) if return_final_state else None
     ws = _ptr(workspace) if ws_bytes else None
+    if return_ckpt:
+        ckpt = torch.empty(((L + 31) // 32, batch, dim, N), dtype=torch.float32, device=x.device)
+        rc = lib.ssm_scan_fwd_ckpt(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                   _ptr(dt_bias), int(bool(delta_softplus)), _ptr(initial_state), _ptr(y), fs,
+                                   _ptr(ckpt), batch, dim, N, L, code, ws, ws_bytes, stream, v)
+        _native.check(rc)
+        return (y, final_state, ckpt) if return_final_state else (y, ckpt)
     if initial_state is None:
         rc = lib.ssm_scan_fwd_variant(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                       _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), fs,
@@ -278,18 +289,27 @@ def scan_bwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
              dy: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
              dt_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
              initial_state: Optional[torch.Tensor] = None, dfinal_state: Optional[torch.Tensor] = None,
-             workspace: Optional[torch.Tensor] = None) -> dict:
+             workspace: Optional[torch.Tensor] = None, ckpt: Optional[torch.Tensor] = None) -> dict:
     """Gradients of the forward (include/ssm_bwd.h) on CUDA tensors, for a
     loss with dL/dy = dy (dtype of x) and dL/dfinal_state = dfinal_state
     (float32, optional).  Returns a dict: dx, ddelta, dz (dtype of x; dz only
     with z), dA, dB, dC, dD (only with D), ddt_bias (only with dt_bias) and
-    dinitial_state (float32)."""
+    dinitial_state (float32).  ``ckpt``: the checkpoints of ``scan_fwd(...,
+    return_ckpt=True)`` over the same inputs (ssm_scan_bwd_ckpt); the start
+    state then enters through them, so ``initial_state`` must be None."""
     batch, dim, N, L = _check_inputs(x, delta, A, B, C, D, z, dt_bias, "cuda")
     if dy.dtype != x.dtype or dy.shape != x.shape or not dy.is_contiguous():
         raise ValueError("dy must be a contiguous tensor like x")
     for name, t in (("initial_state", initial_state), ("dfinal_state", dfinal_state)):
         if t is not None and (t.dtype != torch.float32 or t.shape != (batch, dim, N) or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous float32 [batch, dim, dstate] tensor")
+    if ckpt is not None:
+        if initial_state is not None:
+            raise ValueError("with ckpt the start state enters through the checkpoints: initial_state must be None")
+        if (ckpt.dtype != torch.float32 or ckpt.shape != ((L + 31) // 32, batch, dim, N)
+                or not ckpt.is_contiguous() or ckpt.device != x.device):
+            raise ValueError("ckpt must be the contiguous float32 [ceil(L / 32), batch, dim, dstate] "
+                             "checkpoints of scan_fwd(..., return_ckpt=True)")
     lib = _native.load()
     code = _dtype_code(x.dtype)
     f32 = dict(dtype=torch.float32, device=x.device)
@@ -298,17 +318,19 @@ def scan_bwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
              dC=torch.empty((batch, N, L), **f32), dD=torch.empty((dim,), **f32) if D is not None else None,
              ddt_bias=torch.empty((dim,), **f32) if dt_bias is not None else None,
              dinitial_state=torch.empty((batch, dim, N), **f32))
-    ws_bytes = lib.ssm_scan_bwd_workspace_size(batch, dim, N, L, code)
+    ws_bytes = (lib.ssm_scan_bwd_ckpt_workspace_size if ckpt is not None else lib.ssm_scan_bwd_workspace_size)(
+        batch, dim, N, L, code)
     if ws_bytes == (1 << 64) - 1:
         raise ScanError(-2, "invalid sizes")
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
-    rc = lib.ssm_scan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
-                          int(bool(delta_softplus)), _ptr(initial_state), _ptr(dy), _ptr(dfinal_state),
-                          _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
-                          _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dinitial_state"]),
-                          batch, dim, N, L, code, _ptr(workspace) if ws_bytes else None, ws_bytes,
-                          torch.cuda.current_stream(x.device).cuda_stream)
+    entry = lib.ssm_scan_bwd_ckpt if ckpt is not None else lib.ssm_scan_bwd
+    rc = entry(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+               int(bool(delta_softplus)), _ptr(ckpt if ckpt is not None else initial_state), _ptr(dy),
+               _ptr(dfinal_state), _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+               _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dinitial_state"]),
+               batch, dim, N, L, code, _ptr(workspace) if ws_bytes else None, ws_bytes,
+               torch.cuda.current_stream(x.device).cuda_stream)
     _native.check(rc)
     return g
 

@@ -54,6 +54,16 @@ SIGNATURES = {
     # x, delta, A, B, C, D, z, dt_bias, softplus, h0, dy, dfinal, dx, ddelta, dA, dB, dC, dD, dz, ddt_bias,
     # dh0, batch, dim, dstate, seqlen, dtype, workspace, bytes, stream
     "ssm_scan_bwd": (_i, [_vp] * 8 + [_i] + [_vp] * 12 + [_i, _i, _i, _i64, _i, _vp, _sz, _vp]),
+    # checkpoints of the training forward, consumed by the backward
+    "ssm_scan_ckpt_size": (_sz, [_i, _i, _i, _i64]),
+    "ssm_scan_fwd_ckpt_workspace_size": (_sz, [_i, _i, _i, _i64, _i, _i]),
+    # x..softplus, initial_state, y, final_state, ckpt, sizes, dtype, workspace, bytes, stream, variant
+    "ssm_scan_fwd_ckpt": (_i, list(_FWD_ARGS[:9]) + [_vp] + list(_FWD_ARGS[9:11]) + [_vp] + list(_FWD_ARGS[11:])
+                          + [_i]),
+    "ssm_scan_bwd_ckpt_workspace_size": (_sz, [_i, _i, _i, _i64, _i]),
+    "ssm_scan_bwd_ckpt_kernel_count": (_i, [_i, _i, _i, _i64]),
+    # as ssm_scan_bwd with ckpt in the place of initial_state
+    "ssm_scan_bwd_ckpt": (_i, [_vp] * 8 + [_i] + [_vp] * 12 + [_i, _i, _i, _i64, _i, _vp, _sz, _vp]),
 }
 
 

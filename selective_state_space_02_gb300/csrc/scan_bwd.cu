@@ -41,7 +41,7 @@
 namespace ssm {
 namespace {
 
-constexpr int kChunk = 32;     // steps per recomputed chunk
+constexpr int kChunk = kCkptSteps;   // steps per recomputed chunk (the forward's checkpoint chunks)
 constexpr int kWarps = 4;      // warps per CTA
 
 struct BwdArgs {
@@ -645,23 +645,56 @@ Span span(const void *q, size_t bytes) {
 }
 bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
+bool valid_bwd_sizes(int batch, int dim, int dstate, int64_t seqlen) {
+    return batch >= 0 && dim >= 0 && dstate >= 1 && dstate <= 64 && seqlen >= 0;
+}
+
+// Bytes of the checkpoints: the state at the start of every kChunk-step chunk.
+size_t ckpt_bytes(int batch, int dim, int dstate, int64_t seqlen) {
+    return (size_t)((seqlen + kChunk - 1) / kChunk) * (size_t)batch * dim * dstate * sizeof(float);
+}
+
+int bwd_impl(const void *x, const void *delta, const float *A, const void *B, const void *C, const float *D,
+             const void *z, const float *dt_bias, int delta_softplus, const float *initial_state,
+             const float *ckpt, const void *dy, const float *dfinal_state, void *dx, void *ddelta, float *dA,
+             float *dB, float *dC, float *dD, void *dz, float *ddt_bias, float *dinitial_state, int batch, int dim,
+             int dstate, int64_t seqlen, int io_dtype, void *workspace, size_t workspace_bytes, void *stream);
+
 }  // namespace
 }  // namespace ssm
 
 extern "C" size_t ssm_scan_bwd_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype) {
     if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return (size_t)-1;
-    if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64 || seqlen < 0) return (size_t)-1;
+    if (!ssm::valid_bwd_sizes(batch, dim, dstate, seqlen)) return (size_t)-1;
     if (batch == 0 || dim == 0 || seqlen == 0) return 0;
     const ssm::Plan pl = ssm::plan_for(batch, dim, dstate, seqlen);
     return ssm::r256(ssm::chunk_states_workspace_bytes(batch, dim, dstate, seqlen, ssm::kChunk)) +
            ssm::seg_bytes(pl, (int64_t)batch * dim, dstate);
 }
 
+extern "C" size_t ssm_scan_bwd_ckpt_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype) {
+    if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return (size_t)-1;
+    if (!ssm::valid_bwd_sizes(batch, dim, dstate, seqlen)) return (size_t)-1;
+    if (batch == 0 || dim == 0 || seqlen == 0) return 0;
+    return ssm::seg_bytes(ssm::plan_for(batch, dim, dstate, seqlen), (int64_t)batch * dim, dstate);
+}
+
+extern "C" size_t ssm_scan_ckpt_size(int batch, int dim, int dstate, int64_t seqlen) {
+    if (!ssm::valid_bwd_sizes(batch, dim, dstate, seqlen)) return (size_t)-1;
+    return ssm::ckpt_bytes(batch, dim, dstate, seqlen);
+}
+
 extern "C" int ssm_scan_bwd_kernel_count(int batch, int dim, int dstate, int64_t seqlen) {
-    if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64 || seqlen < 0) return -1;
+    if (!ssm::valid_bwd_sizes(batch, dim, dstate, seqlen)) return -1;
     if (batch == 0 || dim == 0 || seqlen == 0) return 0;
     const ssm::Plan pl = ssm::plan_for(batch, dim, dstate, seqlen);
     return ssm::chunk_start_states_kernels(batch, dim, dstate, seqlen, ssm::kChunk) + (pl.nseg > 1 ? 3 : 1);
+}
+
+extern "C" int ssm_scan_bwd_ckpt_kernel_count(int batch, int dim, int dstate, int64_t seqlen) {
+    if (!ssm::valid_bwd_sizes(batch, dim, dstate, seqlen)) return -1;
+    if (batch == 0 || dim == 0 || seqlen == 0) return 0;
+    return ssm::plan_for(batch, dim, dstate, seqlen).nseg > 1 ? 3 : 1;
 }
 
 extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, const void *B, const void *C,
@@ -670,9 +703,37 @@ extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, co
                             void *ddelta, float *dA, float *dB, float *dC, float *dD, void *dz, float *ddt_bias,
                             float *dinitial_state, int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                             void *workspace, size_t workspace_bytes, void *stream) {
-    using namespace ssm;
+    return ssm::bwd_impl(x, delta, A, B, C, D, z, dt_bias, delta_softplus, initial_state, nullptr, dy,
+                         dfinal_state, dx, ddelta, dA, dB, dC, dD, dz, ddt_bias, dinitial_state, batch, dim,
+                         dstate, seqlen, io_dtype, workspace, workspace_bytes, stream);
+}
+
+extern "C" int ssm_scan_bwd_ckpt(const void *x, const void *delta, const float *A, const void *B, const void *C,
+                                 const float *D, const void *z, const float *dt_bias, int delta_softplus,
+                                 const float *ckpt, const void *dy, const float *dfinal_state, void *dx,
+                                 void *ddelta, float *dA, float *dB, float *dC, float *dD, void *dz,
+                                 float *ddt_bias, float *dinitial_state, int batch, int dim, int dstate,
+                                 int64_t seqlen, int io_dtype, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+    if (!ckpt && seqlen > 0) return SSM_ERR_NULL;
+    return ssm::bwd_impl(x, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, ckpt, dy, dfinal_state, dx,
+                         ddelta, dA, dB, dC, dD, dz, ddt_bias, dinitial_state, batch, dim, dstate, seqlen,
+                         io_dtype, workspace, workspace_bytes, stream);
+}
+
+namespace ssm {
+namespace {
+
+// The backward: chunk-start states from `ckpt` when given (the checkpoints of
+// the forward), else computed here from the start state into the workspace.
+int bwd_impl(const void *x, const void *delta, const float *A, const void *B, const void *C, const float *D,
+                  const void *z, const float *dt_bias, int delta_softplus, const float *initial_state,
+                  const float *ckpt, const void *dy, const float *dfinal_state, void *dx, void *ddelta, float *dA,
+                  float *dB, float *dC, float *dD, void *dz, float *ddt_bias, float *dinitial_state, int batch,
+                  int dim, int dstate, int64_t seqlen, int io_dtype, void *workspace, size_t workspace_bytes,
+                  void *stream) {
     if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
-    if (batch < 0 || dim < 0 || dstate < 1 || dstate > 64 || seqlen < 0) return SSM_ERR_DIMS;
+    if (!valid_bwd_sizes(batch, dim, dstate, seqlen)) return SSM_ERR_DIMS;
     if (seqlen > ((int64_t)1 << 40) || (int64_t)batch * dim > ((int64_t)1 << 31)) return SSM_ERR_DIMS;
     if (batch == 0 || dim == 0) return SSM_OK;
     if (!A || !dA) return SSM_ERR_NULL;
@@ -682,7 +743,7 @@ extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, co
     const void *iop[] = {x, delta, B, C, z, dy, dx, ddelta, dz};
     for (const void *q : iop)
         if (q && !aligned(q, es)) return SSM_ERR_ALIGN;
-    const void *fp[] = {A, D, dt_bias, initial_state, dfinal_state, dA, dB, dC, dD, ddt_bias, dinitial_state};
+    const void *fp[] = {A, D, dt_bias, initial_state, ckpt, dfinal_state, dA, dB, dC, dD, ddt_bias, dinitial_state};
     for (const void *q : fp)
         if (q && !aligned(q, 4)) return SSM_ERR_ALIGN;
     const size_t nx = (size_t)batch * dim * (size_t)seqlen * es;
@@ -690,7 +751,8 @@ extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, co
     const size_t ns = (size_t)batch * dim * dstate * 4;
     const Span ins[] = {span(x, nx), span(delta, nx), span(z, nx), span(B, nb * es), span(C, nb * es),
                         span(A, (size_t)dim * dstate * 4), span(D, (size_t)dim * 4), span(dt_bias, (size_t)dim * 4),
-                        span(initial_state, ns), span(dy, nx), span(dfinal_state, ns)};
+                        span(initial_state, ns), span(dy, nx), span(dfinal_state, ns),
+                        span(ckpt, ckpt_bytes(batch, dim, dstate, seqlen))};
     const Span outs[] = {span(dx, nx), span(ddelta, nx), span(z ? dz : nullptr, nx), span(dA, (size_t)dim * dstate * 4),
                          span(dB, nb * 4), span(dC, nb * 4), span(D ? dD : nullptr, (size_t)dim * 4),
                          span(ddt_bias, (size_t)dim * 4), span(dinitial_state, ns)};
@@ -700,7 +762,8 @@ extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, co
         for (const Span &o2 : outs)
             if (&o != &o2 && overlap(o, o2)) return SSM_ERR_ALIAS;
     }
-    const size_t need = ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen, io_dtype);
+    const size_t need = ckpt ? ssm_scan_bwd_ckpt_workspace_size(batch, dim, dstate, seqlen, io_dtype)
+                             : ssm_scan_bwd_workspace_size(batch, dim, dstate, seqlen, io_dtype);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return SSM_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the accumulated gradients start from zero
@@ -729,14 +792,21 @@ extern "C" int ssm_scan_bwd(const void *x, const void *delta, const float *A, co
     for (const void *q : rows)
         if (!aligned(q, 16)) v16 = false;
     f.vec16 = v16 ? 1 : 0;
-    if (chunk_start_states(f, kChunk, workspace, st) != cudaSuccess) return SSM_ERR_LAUNCH;
     const Plan pl = plan_for(batch, dim, dstate, seqlen);
-    char *seg_ws = static_cast<char *>(workspace) +
-                   r256(chunk_states_workspace_bytes(batch, dim, dstate, seqlen, kChunk));
-    BwdArgs a{x, delta, A, B, C, D, z, dt_bias, delta_softplus ? 1 : 0, static_cast<const float *>(workspace),
+    char *seg_ws = static_cast<char *>(workspace);
+    const float *states = ckpt;
+    if (!ckpt) {
+        if (chunk_start_states(f, kChunk, workspace, st) != cudaSuccess) return SSM_ERR_LAUNCH;
+        states = static_cast<const float *>(workspace);
+        seg_ws += r256(chunk_states_workspace_bytes(batch, dim, dstate, seqlen, kChunk));
+    }
+    BwdArgs a{x, delta, A, B, C, D, z, dt_bias, delta_softplus ? 1 : 0, states,
               dy, nullptr, 1, dx, ddelta, dA, dB, dC, D ? dD : nullptr, z ? dz : nullptr, ddt_bias,
               dinitial_state, batch, dim, dstate, seqlen};
     const cudaError_t e = io_dtype == SSM_BF16 ? launch_t<__nv_bfloat16>(a, pl, dfinal_state, seg_ws, st)
                                                : launch_t<float>(a, pl, dfinal_state, seg_ws, st);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
+
+}  // namespace
+}  // namespace ssm

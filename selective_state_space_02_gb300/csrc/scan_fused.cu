@@ -135,6 +135,10 @@ cudaError_t launch_mode(const FwdArgs &a, const fused::SegArgs &sg, int mode, in
     if (!status) return cudaErrorInvalidSymbol;
     fused::TileMaps maps;
     const bool tma = make_maps(a, cfg, sg.bc, maps);
+    if (a.ckpt && (mode == fused::kWhole || mode == fused::kSeeded)) {   // the forward's y pass with checkpoints
+        if (a.bf16) return fused::launch_typed_ckpt<__nv_bfloat16>(a, sg, maps, status, mode, tma, cfg, prepare, st);
+        return fused::launch_typed_ckpt<float>(a, sg, maps, status, mode, tma, cfg, prepare, st);
+    }
     if (a.bf16) return fused::launch_typed<__nv_bfloat16>(a, sg, maps, status, mode, tma, cfg, prepare, st);
     return fused::launch_typed<float>(a, sg, maps, status, mode, tma, cfg, prepare, st);
 }
@@ -272,7 +276,7 @@ size_t fused_workspace_bytes(int batch, int dim, int dstate, int64_t L) {
 
 cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t st) {
     const int64_t nchan = (int64_t)a.batch * a.dim;
-    fused::SegArgs sg{a.L, 1, nullptr, nullptr, static_cast<const float *>(workspace)};
+    fused::SegArgs sg{a.L, 1, nullptr, nullptr, static_cast<const float *>(workspace), kCkptSteps};
     return launch_mode(a, sg, fused::kWhole, choose_cfg(nchan, padded_states(a.dstate), 1), true, st);
 }
 
@@ -319,7 +323,7 @@ cudaError_t launch_twopass(const FwdArgs &a, void *workspace, cudaStream_t st) {
     sbytes = (sbytes + 255) / 256 * 256;
     char *ws = static_cast<char *>(workspace);
     fused::SegArgs sg{len, nseg, reinterpret_cast<float *>(ws), reinterpret_cast<float *>(ws + hbytes),
-                      reinterpret_cast<const float *>(ws + hbytes + sbytes)};
+                      reinterpret_cast<const float *>(ws + hbytes + sbytes), kCkptSteps};
     const int cfg = twopass_cfg(padded_states(a.dstate));
     cudaError_t e = cudaSuccess;
     bool prepared = false;

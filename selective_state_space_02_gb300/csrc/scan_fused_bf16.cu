@@ -6,7 +6,7 @@ namespace fused {
 template <>
 cudaError_t launch_typed<__nv_bfloat16>(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, unsigned int *status,
                              int mode, bool tma, int cfg, bool prepare, cudaStream_t st) {
-    return launch_typed_impl<__nv_bfloat16>(a, sg, maps, status, mode, tma, cfg, prepare, st);
+    return launch_typed_impl<__nv_bfloat16, false>(a, sg, maps, status, mode, tma, cfg, prepare, st);
 }
 }  // namespace fused
 }  // namespace ssm

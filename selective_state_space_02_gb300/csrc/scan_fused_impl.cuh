@@ -77,7 +77,8 @@ struct SegArgs {
     float *ws_h;       // [nseg][batch*dim][dstate]: B_k after pass 1, h_init after the small scan
     float *ws_s;       // [nseg][batch*dim]: sum of Delta over the segment
     const float *bc;   // prepared B/C rows [batch*L][bc_row(NP, S)]
-    int64_t ck_len;    // kStates: steps per chunk (whole tiles); ws_h is then [nchunk][batch*dim][dstate]
+    int64_t ck_len;    // kStates, or kWhole/kSeeded with checkpoints (FwdArgs::ckpt): steps per chunk
+                       // (whole tiles); the states are then [nchunk][batch*dim][dstate] (kStates: in ws_h)
 };
 
 // Floats per prepared B/C row: NS groups of S B values and S C values.  A
@@ -362,11 +363,16 @@ struct ReduceScatter<LEN, 0> {
     static __device__ __forceinline__ void run(float (&)[NV], int) {}
 };
 
-template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA, int CK = 0>
-__global__ void __launch_bounds__((NW + 1) * 32, 1)
+// CKPT: the forward also stores its checkpoints (FwdArgs::ckpt), the state at
+// the start of every kCkptSteps-step chunk; separate instantiations, so that
+// the plain forward carries none of it.  Those keep 16-state lanes at 3 CTAs
+// per SM, as the plain kernel's registers allow.
+template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA, int CK = 0, bool CKPT = false>
+__global__ void __launch_bounds__((NW + 1) * 32, (CKPT && S >= 16) ? 3 : 1)
 scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps maps, unsigned int *status) {
     using Ly = Layout<T, NP, S, NW, GATE, MODE, CK>;
     static_assert(CK == 0 || (MODE == kWhole && CK <= 4), "the convolution runs with whole sequences");
+    static_assert(!CKPT || ((MODE == kWhole || MODE == kSeeded) && CK == 0), "checkpoints of the y passes");
     constexpr int NS = Ly::NS, CPW = Ly::CPW, DT = Ly::DT, E = Ly::E, TC = Ly::TC;
     constexpr bool kY = Ly::kY, kZ = Ly::kZ;
     static_assert(S % 2 == 0 && (NS == 1 || NS == 2 || NS == 4 || NS == 8), "lane split");
@@ -539,10 +545,13 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
         const int tvalid = (int)((te - t0) < TC ? (te - t0) : TC);
         const bool ok = wait_parity(&full[st], (uint32_t)((tile / kNST) & 1), status);
         if (!__all_sync(FULL, ok && *abort_flag == 0)) { aborted = true; break; }
-        if constexpr (MODE == kStates) {
-            // the state at the start of every ck_len-step chunk
-            if (dok && t0 % sg.ck_len == 0) {
-                float *dst = sg.ws_h + ((t0 / sg.ck_len) * nchan + chan0 + d) * N;
+        if constexpr (MODE == kStates || CKPT) {
+            // the state at the start of every chunk: the state pass's output
+            // (ck_len-step chunks), or the forward's checkpoints (kCkptSteps)
+            float *const ck = MODE == kStates ? sg.ws_h : p.ckpt;
+            const int64_t ckl = MODE == kStates ? sg.ck_len : (int64_t)kCkptSteps;
+            if (dok && t0 % ckl == 0) {
+                float *dst = ck + ((t0 / ckl) * nchan + chan0 + d) * N;
 #pragma unroll
                 for (int q = 0; q < S / 2; ++q) {
                     const int n = g * S + 2 * q;
@@ -718,11 +727,11 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
 }
 
 // Launch one instantiation.
-template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA, int CK = 0>
+template <typename T, int NP, int S, int NW, bool GATE, int MODE, bool TMA, int CK = 0, bool CKPT = false>
 cudaError_t launch_one(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, unsigned int *status,
                        cudaStream_t st) {
     using Ly = Layout<T, NP, S, NW, GATE, MODE, CK>;
-    auto kern = scan_kernel<T, NP, S, NW, GATE, MODE, TMA, CK>;
+    auto kern = scan_kernel<T, NP, S, NW, GATE, MODE, TMA, CK, CKPT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ly::bytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.dim + Ly::DT - 1) / Ly::DT), (unsigned)a.batch, (unsigned)sg.nseg);
@@ -743,6 +752,11 @@ cudaError_t launch_prepare(const FwdArgs &a, float *out, cudaStream_t st) {
 template <typename T>
 cudaError_t launch_typed(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, unsigned int *status,
                          int mode, bool tma, int cfg, bool prepare, cudaStream_t st);
+// The same for the forward that stores checkpoints (kWhole and kSeeded only;
+// defined in scan_fused_ckpt_<type>.cu).
+template <typename T>
+cudaError_t launch_typed_ckpt(const FwdArgs &a, const SegArgs &sg, const TileMaps &maps, unsigned int *status,
+                              int mode, bool tma, int cfg, bool prepare, cudaStream_t st);
 
 }  // namespace fused
 }  // namespace ssm

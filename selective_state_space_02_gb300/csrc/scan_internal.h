@@ -34,7 +34,14 @@ struct FwdArgs {
     const float *conv_w = nullptr;       // [dim, conv_k]
     const float *conv_b = nullptr;       // nullable [dim]
     const void *conv_state = nullptr;    // nullable [batch, dim, conv_k - 1], io dtype: inputs before t = 0
+    // nullable: checkpoints for the backward, the state at the start of every
+    // kCkptSteps-step chunk, [nchunk][batch*dim][dstate] float32 (FUSED and
+    // TWOPASS variants)
+    float *ckpt = nullptr;
 };
+
+// Steps per checkpointed chunk: the chunk length of the backward's recomputation.
+constexpr int kCkptSteps = 32;
 
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_fused(const FwdArgs &a, void *workspace, cudaStream_t s);

@@ -24,6 +24,14 @@ int resolve_variant(int batch, int dim, int dstate, int64_t seqlen, int io_dtype
     return variant;
 }
 
+// The variant of a forward that writes checkpoints: FUSED and TWOPASS store
+// them as they go; where AUTO would pick CHUNKED it takes TWOPASS.
+int ckpt_variant(int batch, int dim, int dstate, int64_t seqlen, int io_dtype, int variant) {
+    const int v = resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant);
+    if (v != SSM_VARIANT_CHUNKED) return v;
+    return variant == SSM_VARIANT_AUTO ? SSM_VARIANT_TWOPASS : SSM_ERR_UNSUPPORTED;
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Range {
@@ -228,6 +236,15 @@ size_t ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int64_t seqle
     return workspace_for(batch, dim, dstate, seqlen, v);
 }
 
+size_t ssm_scan_fwd_ckpt_workspace_size(int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
+                                        int variant) {
+    if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return (size_t)-1;
+    if (!valid_sizes(batch, dim, dstate, seqlen)) return (size_t)-1;
+    const int v = ckpt_variant(batch, dim, dstate, seqlen, io_dtype, variant);
+    if (v < 0) return (size_t)-1;
+    return workspace_for(batch, dim, dstate, seqlen, v);
+}
+
 }  // extern "C"
 
 namespace {
@@ -248,11 +265,26 @@ int fwd_device(const void *x, const void *delta, const float *A, const void *B, 
                const void *z, const float *dt_bias, int delta_softplus, const float *h0, void *y,
                float *final_state, int batch, int dim, int dstate, int64_t seqlen, int io_dtype,
                void *workspace, size_t workspace_bytes, void *stream, int variant,
-               const ConvArgs &conv = ConvArgs{}) {
+               const ConvArgs &conv = ConvArgs{}, float *ckpt = nullptr) {
     int rc = validate(x, delta, A, B, C, D, z, dt_bias, y, final_state, batch, dim, dstate, seqlen,
                       io_dtype, h0);
     if (rc != SSM_OK) return rc;
-    const int v = resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant);
+    if (ckpt) {   // the checkpoints overlap nothing else
+        if (!aligned(ckpt, 4)) return SSM_ERR_ALIGN;
+        const size_t es = elem_size(io_dtype);
+        const size_t nx = (size_t)batch * dim * (size_t)seqlen * es;
+        const size_t nb = (size_t)batch * dstate * (size_t)seqlen * es;
+        const size_t ns = (size_t)batch * dim * dstate * 4;
+        const Range ck = range_of(ckpt, ssm_scan_ckpt_size(batch, dim, dstate, seqlen));
+        const Range others[] = {range_of(x, nx), range_of(delta, nx), range_of(z, z ? nx : 0),
+                                range_of(B, nb), range_of(C, nb), range_of(A, (size_t)dim * dstate * 4),
+                                range_of(D, D ? (size_t)dim * 4 : 0), range_of(dt_bias, dt_bias ? (size_t)dim * 4 : 0),
+                                range_of(h0, h0 ? ns : 0), range_of(y, nx), range_of(final_state, final_state ? ns : 0)};
+        for (const Range &o : others)
+            if (overlap(ck, o)) return SSM_ERR_ALIAS;
+    }
+    const int v = ckpt ? ckpt_variant(batch, dim, dstate, seqlen, io_dtype, variant)
+                       : resolve_variant(batch, dim, dstate, seqlen, io_dtype, variant);
     if (v < 0) return v;
     const size_t need = workspace_for(batch, dim, dstate, seqlen, v);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
@@ -284,6 +316,7 @@ int fwd_device(const void *x, const void *delta, const float *A, const void *B, 
     a.conv_w = conv.w;
     a.conv_b = conv.b;
     a.conv_state = conv.state;
+    a.ckpt = ckpt;
     if (conv.conv_k > 0 && v != SSM_VARIANT_FUSED) return SSM_ERR_UNSUPPORTED;
     cudaError_t e;
     switch (v) {
@@ -315,6 +348,17 @@ int ssm_scan_fwd_from_state(const void *x, const void *delta, const float *A, co
                             void *workspace, size_t workspace_bytes, void *stream, int variant) {
     return fwd_device(x, delta, A, B, C, D, z, dt_bias, delta_softplus, initial_state, y, final_state, batch,
                       dim, dstate, seqlen, io_dtype, workspace, workspace_bytes, stream, variant);
+}
+
+int ssm_scan_fwd_ckpt(const void *x, const void *delta, const float *A, const void *B, const void *C,
+                      const float *D, const void *z, const float *dt_bias, int delta_softplus,
+                      const float *initial_state, void *y, float *final_state, float *ckpt, int batch, int dim,
+                      int dstate, int64_t seqlen, int io_dtype, void *workspace, size_t workspace_bytes,
+                      void *stream, int variant) {
+    if (!ckpt && batch > 0 && dim > 0 && seqlen > 0) return SSM_ERR_NULL;
+    return fwd_device(x, delta, A, B, C, D, z, dt_bias, delta_softplus, initial_state, y, final_state, batch,
+                      dim, dstate, seqlen, io_dtype, workspace, workspace_bytes, stream, variant, ConvArgs{},
+                      ckpt);
 }
 
 int ssm_scan_fwd(const void *x, const void *delta, const float *A, const void *B, const void *C,

@@ -286,3 +286,34 @@ def test_backward_chunk_state_route_boundary(lib):
     assert f(2, 1216, 13, 4096) == 5 and f(2, 1214, 13, 4096) == 6   # padded states count like 16
     # 64 states: 4864 channels = 608 warps; one walk
     assert f(1, 4864, 64, 64) == 3 and f(1, 4856, 64, 64) == 4
+
+
+def test_checkpoint_sizes_and_refusals(lib):
+    """The training pair's host side: checkpoint bytes (ceil(L / 32) chunk
+    states), the forward's workspace (that of the variant it runs; none for
+    CHUNKED), the backward's (segment sums only) and kernel count, and the
+    checks that refuse before anything is launched."""
+    SIZE_MAX = (1 << 64) - 1
+    assert lib.ssm_scan_ckpt_size(4, 1536, 16, 2048) == 64 * 4 * 1536 * 16 * 4
+    assert lib.ssm_scan_ckpt_size(2, 9, 5, 130) == 5 * 2 * 9 * 5 * 4
+    assert lib.ssm_scan_ckpt_size(1, 8, 16, 0) == 0 and lib.ssm_scan_ckpt_size(1, 8, 65, 10) == SIZE_MAX
+    fws = lib.ssm_scan_fwd_ckpt_workspace_size
+    plain = lib.ssm_scan_fwd_workspace_size
+    assert fws(4, 1536, 16, 2048, 1, 1) == plain(4, 1536, 16, 2048, 1, 1)         # FUSED
+    assert fws(2, 9, 5, 130, 0, 3) == plain(2, 9, 5, 130, 0, 3)                     # TWOPASS
+    assert lib.ssm_scan_select_variant(2, 9, 5, 130, 0) == 2                        # AUTO: CHUNKED ...
+    assert fws(2, 9, 5, 130, 0, 0) == plain(2, 9, 5, 130, 0, 3)                     # ... taken as TWOPASS
+    assert fws(2, 9, 5, 130, 0, 2) == SIZE_MAX                                      # CHUNKED: none
+    assert lib.ssm_scan_bwd_ckpt_workspace_size(4, 1536, 16, 2048, 1) == 0          # one segment
+    assert lib.ssm_scan_bwd_ckpt_workspace_size(1, 768, 16, 131072, 0) > 0         # segments
+    assert lib.ssm_scan_bwd_ckpt_kernel_count(4, 1536, 16, 2048) == 1
+    assert lib.ssm_scan_bwd_ckpt_kernel_count(1, 768, 16, 131072) == 3
+    assert lib.ssm_scan_bwd_ckpt_kernel_count(0, 8, 16, 20) == 0
+    # no checkpoint buffer: refused before any launch (no pointer is dereferenced)
+    ERR_NULL = -1
+    rc = lib.ssm_scan_fwd_ckpt(16, 16, 16, 16, 16, None, None, None, 1, None, 16, None, None,
+                               1, 8, 16, 64, 0, None, 0, None, 1)
+    assert rc == ERR_NULL
+    rc = lib.ssm_scan_bwd_ckpt(16, 16, 16, 16, 16, None, None, None, 1, None, 16, None, 16, 16, 16, 16, 16,
+                               None, None, None, None, 1, 8, 16, 64, 0, None, 0, None)
+    assert rc == ERR_NULL
