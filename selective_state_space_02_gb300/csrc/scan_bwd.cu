@@ -4,11 +4,13 @@
 // state sequence; the backward reads the state at the start of each chunk and
 // recomputes the chunk's states from it while walking the chunks in reverse.
 //
-// 1. Chunk-start states (chunk_start_states in scan_fused.cu): h at the start
-//    of every chunk, from the start state -- stored by one whole-sequence
-//    pass of the fused forward where the channels fill the GPU, else from
-//    the two-pass forward's totals pass and carry scan with segments of
-//    kChunk steps.
+// 1. Chunk-start states: h at the start of every chunk.  The training
+//    forward (ssm_scan_fwd_ckpt) stores them as it runs, and
+//    ssm_scan_bwd_ckpt starts from those; otherwise chunk_start_states
+//    (scan_fused.cu) computes them from the start state -- by one
+//    whole-sequence pass of the fused forward where the channels fill the
+//    GPU, else by the two-pass forward's totals pass and carry scan with
+//    segments of kChunk steps.
 // 2. bwd_kernel: a CTA owns CPC channels of one batch (LPC lanes per channel,
 //    S2 states per lane) and walks their chunks from the last to the first.
 //    The two serial chains are kept minimal and everything else is done by

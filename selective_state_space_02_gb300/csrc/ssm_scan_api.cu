@@ -9,7 +9,7 @@
 
 namespace {
 
-constexpr int kVersion = (1 << 16) | 1;
+constexpr int kVersion = (1 << 16) | 2;
 constexpr int kFusedConvTaps = 4;   // widest filter the fused kernel takes
 
 bool valid_sizes(int batch, int dim, int dstate, int64_t seqlen) {
