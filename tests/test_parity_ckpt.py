@@ -121,7 +121,8 @@ def test_backward_from_checkpoints(case):
     _compare(g, ref, dt)
 
 
-def test_start_state_through_checkpoints():
+@pytest.mark.parametrize("variant", ["fused", "twopass"])
+def test_start_state_through_checkpoints(variant):
     """A start state and a final-state gradient: the forward's checkpoints
     carry the start state (entry 0 is h0), the backward from them gives the
     start state's gradient."""
@@ -129,7 +130,7 @@ def test_start_state_through_checkpoints():
     h0 = synth.make_state(2, 24, 16, seed=831)
     dfinal = synth.make_state(2, 24, 16, seed=832)
     t = _dev(p)
-    y, fs, ck = _fwd(t, p, "fused", h0=h0.cuda())
+    y, fs, ck = _fwd(t, p, variant, h0=h0.cuda())
     torch.cuda.synchronize()
     assert torch.equal(ck[0].cpu(), h0)
     ref = _oracle_chunk_states(p, h0)
