@@ -99,7 +99,13 @@ struct Shape {
     static_assert(TR % 16 == 2, "term row stride");
     static constexpr int o_in = 0;                           // float4 [CPC][IR]: Delta, u, dq, x
     static constexpr int o_sz = o_in + 4 * IR * CPC;         // float2 [CPC][IR]: softplus'(v), dy silu'(z)
-    static constexpr int o_bc = o_sz + 2 * IR * CPC;         // [kChunk][BR] records of 2 S2 floats: the B, then the C of a lane's states
+    // B and C of a lane's states per step: interleaved records of 2 S2 floats
+    // (the B, then the C) for 8 lanes a channel, where a warp reads 8 distinct
+    // records; separate B and C rows for 32 lanes a channel, where the B-only
+    // reads of the recomputation would otherwise find the B halves of the
+    // records on half the banks (a 4-way conflict)
+    static constexpr bool kSplit = LPC == 32;
+    static constexpr int o_bc = o_sz + 2 * IR * CPC;         // [kChunk][BR] records, or [kChunk][BR] B then C
     static constexpr int o_tb = o_bc + 2 * S2 * kChunk * BR; // float2 [F][TR]: per-(channel, state) dB, dC terms
     static constexpr int o_bias = o_tb + 2 * F * TR;         // float [CPC]: dt_bias of the CTA's channels
     static constexpr size_t bytes = (size_t)(o_bias + CPC) * 4;
@@ -242,7 +248,9 @@ __global__ void __launch_bounds__(kWarps * 32, MINB) bwd_kernel(const BwdArgs p)
     using Ln = Lane<S2>;
     using V = typename Ln::V;
     using Rec = typename Ln::Rec;
-    Rec *bc = reinterpret_cast<Rec *>(sm + Sh::o_bc);         // [kChunk][BR]
+    Rec *bc = reinterpret_cast<Rec *>(sm + Sh::o_bc);         // [kChunk][BR] records (not kSplit)
+    V *bsp = reinterpret_cast<V *>(sm + Sh::o_bc);             // kSplit: [kChunk][BR] B, then
+    V *csp = bsp + kChunk * BR;                                //         [kChunk][BR] C
     float2 *tb = reinterpret_cast<float2 *>(sm + Sh::o_tb);   // [F][TR]
     float *sbias = sm + Sh::o_bias;                            // [CPC]
     const int tid = threadIdx.x;
@@ -323,7 +331,12 @@ __global__ void __launch_bounds__(kWarps * 32, MINB) bwd_kernel(const BwdArgs p)
                 bv[s] = ok ? of_bits<T>(raw.B[i * S2 + s]) : 0.0f;
                 cv[s] = ok ? of_bits<T>(raw.C[i * S2 + s]) : 0.0f;
             }
-            bc[j * BR + l] = Ln::rec(bv, cv);
+            if constexpr (Sh::kSplit) {
+                bsp[j * BR + l] = Ln::make(bv);
+                csp[j * BR + l] = Ln::make(cv);
+            } else {
+                bc[j * BR + l] = Ln::rec(bv, cv);
+            }
         }
         const V hst = Ln::make(hnext);                      // the chunk's start state
         __syncthreads();
@@ -337,6 +350,7 @@ __global__ void __launch_bounds__(kWarps * 32, MINB) bwd_kernel(const BwdArgs p)
         for (int sub = kChunk / SC - 1; sub >= 0; --sub) {
             const int j0 = sub * SC;
             const Rec *bcl = bc + li;                       // the lane's records, row stride BR
+            const V *bsl = bsp + li, *csl = csp + li;       // kSplit: the lane's B and C, row stride BR
             V h[SC + 1];                                    // h[j + 1] = state after step j0 + j
             V av[SC];                                       // av[j] = a of step j0 + j (for the adjoint)
             h[0] = hst;
@@ -344,14 +358,15 @@ __global__ void __launch_bounds__(kWarps * 32, MINB) bwd_kernel(const BwdArgs p)
             for (int j = 0; j < j0; ++j) {
                 const float4 q = in[c * IR + j];
                 h[0] = Ln::fma(Ln::exp2(Ln::mul(Ln::splat(q.x), A2)), h[0],
-                               Ln::mul(Ln::splat(q.y), Ln::load_B(bcl + j * BR)));
+                               Ln::mul(Ln::splat(q.y), Sh::kSplit ? bsl[j * BR] : Ln::load_B(bcl + j * BR)));
             }
             // ---- b. recompute the sub-chunk's states into registers ----------
 #pragma unroll
             for (int j = 0; j < SC; ++j) {
                 const float4 q = in[c * IR + j0 + j];
                 av[j] = Ln::exp2(Ln::mul(Ln::splat(q.x), A2));
-                h[j + 1] = Ln::fma(av[j], h[j], Ln::mul(Ln::splat(q.y), Ln::load_B(bcl + (j0 + j) * BR)));
+                const V bj = Sh::kSplit ? bsl[(j0 + j) * BR] : Ln::load_B(bcl + (j0 + j) * BR);
+                h[j + 1] = Ln::fma(av[j], h[j], Ln::mul(Ln::splat(q.y), bj));
             }
             // ---- c. the adjoint backwards, F steps between reductions ----------
 #pragma unroll
@@ -367,12 +382,20 @@ __global__ void __launch_bounds__(kWarps * 32, MINB) bwd_kernel(const BwdArgs p)
                     const int jl = f * F + jj;                  // step within the sub-chunk
                     const int j = j0 + jl;
                     const float4 q = in[c * IR + j];
-                    const Rec r = bcl[j * BR];
-                    const V Cv = Ln::C(r), a = av[jl], hn = h[jl + 1];
+                    V Bv, Cv;
+                    if constexpr (Sh::kSplit) {
+                        Bv = bsl[j * BR];
+                        Cv = csl[j * BR];
+                    } else {
+                        const Rec r = bcl[j * BR];
+                        Bv = Ln::B(r);
+                        Cv = Ln::C(r);
+                    }
+                    const V a = av[jl], hn = h[jl + 1];
                     lam = Ln::fma(Ln::splat(q.z), Cv, lam);
                     const V daa = Ln::mul(Ln::mul(lam, h[jl]), a);  // (dL/da_t) a_t
                     dAacc = Ln::fma(daa, Ln::splat(q.x), dAacc);
-                    const V du = Ln::mul(lam, Ln::B(r)), ds = Ln::mul(daa, Av), pp = Ln::mul(Cv, hn);
+                    const V du = Ln::mul(lam, Bv), ds = Ln::mul(daa, Av), pp = Ln::mul(Cv, hn);
 #pragma unroll
                     for (int s = 0; s < S2; ++s)
                         tb[jj * TR + c * Sh::CS + li + LPC * s] = make_float2(Ln::at(lam, s) * q.y, q.z * Ln::at(hn, s));
