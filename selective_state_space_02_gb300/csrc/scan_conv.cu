@@ -3,12 +3,16 @@
 // sect. 4.1.  Declared in include/ssm_conv.h.
 //
 // The operation reads x once and writes y once, so it is bound by HBM
-// bandwidth.  A thread produces U x G = 16 consecutive outputs of one
-// channel: U vector loads bring its inputs (16 bytes of bf16, 32 of float32,
-// each), one more the neighbouring run's last group whose last K-1 inputs
-// precede them (an L1/L2 hit: its owner loads the same bytes), or the start
-// history for the first run, and U vector stores write the outputs.  The tap count K is a template parameter so that the
-// input window and the taps stay in registers.
+// bandwidth.  A thread produces U x G consecutive outputs of one channel: U
+// vector loads bring its inputs (16 bytes of bf16, 32 of float32, each) and
+// are all issued before the first is used; one more brings the neighbouring
+// run's last group, whose last K-1 inputs precede them (an L1/L2 hit: its
+// owner loads the same bytes), or the start history for the first run; U
+// vector stores write the outputs.  The loaded vectors stay packed until
+// their turn, so that bf16 runs hold twice the vectors (U = 4: 64 bytes in
+// flight per thread, like float32's U = 2) in about as many registers.  The
+// tap count K is a template parameter so that the input window and the taps
+// stay in registers.
 #include "../../include/ssm_conv.h"
 #include "../../include/ssm_scan.h"
 #include "scan_device.cuh"
@@ -18,7 +22,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int G = 8;   // outputs per vector
-constexpr int U = 2;   // vectors per thread
+// vectors per thread: 64 bytes of input in flight for either type
+template <typename T> constexpr int runs_of() { return sizeof(T) == 2 ? 4 : 2; }
 
 struct ConvArgs {
     const void *x;
@@ -68,6 +73,34 @@ template <> struct Vec8<__nv_bfloat16> {
     }
 };
 
+// 8 consecutive I/O elements as loaded (16-byte aligned), expanded to float32
+// only when they are used.
+template <typename T> struct Raw8;
+template <> struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void ld(const void *p, int64_t i) {
+        a = *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+        b = *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i + 4);
+    }
+    __device__ __forceinline__ void get(float *v) const {
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+template <> struct Raw8<__nv_bfloat16> {
+    uint4 w;
+    __device__ __forceinline__ void ld(const void *p, int64_t i) {
+        w = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p) + i);
+    }
+    __device__ __forceinline__ void get(float *v) const {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __uint_as_float(ws[k] << 16);
+            v[2 * k + 1] = __uint_as_float(ws[k] & 0xffff0000u);
+        }
+    }
+};
+
 // SiLU of an output stored in I/O type T: the accurate form for float32; for
 // bf16 outputs the one-instruction form z/2 (1 + tanh(z/2)), whose ~2^-11
 // relative error is far below bf16 rounding (one special-function operation
@@ -97,61 +130,100 @@ __device__ __forceinline__ float stream_at(const ConvArgs &p, int64_t ch, int64_
 // channels (blockDim.x is the run count rounded up to a warp, at most
 // kThreads), grid y over blocks of channels with a stride loop, so no thread
 // divides an index.  A thread issues its U vector loads before it needs them.
+// The K-1 history, G inputs and G outputs of one vector of steps.
+template <typename T, int K>
+__device__ __forceinline__ void conv_vector(const float (&win)[K - 1 + G], const float (&wk)[K], float bias,
+                                            int silu, float (&out)[G]) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        float acc = bias;
+#pragma unroll
+        for (int k = 0; k < K; ++k) acc = fmaf(wk[k], win[j + k], acc);
+        out[j] = silu ? silu_out<T>(acc) : acc;
+    }
+}
+
+// Five CTAs of 256 threads per SM (at most 48 registers): the U vectors in
+// flight stay packed, the window of one vector is expanded at a time.
 template <typename T, int K, bool VEC>
-__global__ void __launch_bounds__(kThreads) conv_kernel(const ConvArgs p) {
+__global__ void __launch_bounds__(kThreads, 5) conv_kernel(const ConvArgs p) {
+    constexpr int U = runs_of<T>();
+    constexpr int KH = K > 1 ? K - 1 : 1;                // the window's history (K - 1 inputs)
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // run of U groups
     const int64_t g0 = r * U;
     if (g0 >= p.ngroups) return;                         // no block-wide synchronisation below
     const int64_t L = p.L;
+    const int64_t t0 = g0 * G;
     for (int64_t ch = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; ch < p.nchan;
          ch += (int64_t)gridDim.y * blockDim.y) {
         const int d = (int)(ch % p.dim);
-        float win[K - 1 + U * G];                        // inputs t0-K+1 .. t0+U*G-1, t0 = g0 * G
+        float hist[KH];                                  // the K-1 inputs before the vector in turn
+        if (VEC && t0 + U * G <= L) {
+            // the whole run inside the row: its U loads first
+            Raw8<T> raw[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t t = (g0 + u) * G;
-            float *dst = win + K - 1 + u * G;
-            if (VEC && t + G <= L) {
-                Vec8<T>::ld(p.x, ch * L + t, dst);
-            } else {
+            for (int u = 0; u < U; ++u) raw[u].ld(p.x, ch * L + t0 + u * G);
+            if (K > 1) {
+                if (g0 > 0) {
+                    Raw8<T> pv;
+                    pv.ld(p.x, ch * L + t0 - G);         // the neighbouring run's last group: an L1/L2 hit
+                    float prev[G];
+                    pv.get(prev);
 #pragma unroll
-                for (int j = 0; j < G; ++j) dst[j] = t + j < L ? Io<T>::ld(p.x, ch * L + t + j) : 0.0f;
+                    for (int k = 0; k < K - 1; ++k) hist[k] = prev[G - (K - 1) + k];
+                } else {
+#pragma unroll
+                    for (int k = 0; k < K - 1; ++k) hist[k] = stream_at<T, K>(p, ch, t0 - (K - 1) + k);
+                }
             }
-        }
-        const int64_t t0 = g0 * G;
-        if (K > 1) {
-            if (VEC && g0 > 0) {
-                float prev[G];
-                Vec8<T>::ld(p.x, ch * L + t0 - G, prev);  // the neighbouring run's last group: an L1/L2 hit
+            float wk[K];
 #pragma unroll
-                for (int k = 0; k < K - 1; ++k) win[k] = prev[G - (K - 1) + k];
-            } else {
+            for (int k = 0; k < K; ++k) wk[k] = __ldg(p.w + (int64_t)d * K + k);
+            const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
 #pragma unroll
-                for (int k = 0; k < K - 1; ++k) win[k] = stream_at<T, K>(p, ch, t0 - (K - 1) + k);
+            for (int u = 0; u < U; ++u) {
+                float win[K - 1 + G], out[G];
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k) win[k] = hist[k];
+                raw[u].get(win + K - 1);
+                conv_vector<T, K>(win, wk, bias, p.silu, out);
+                Vec8<T>::st(p.y, ch * L + t0 + u * G, out);
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k) hist[k] = win[G + k];
             }
-        }
-        float wk[K];
+        } else {
+            // the row's last run, or rows not 16-byte aligned: one vector at a time
 #pragma unroll
-        for (int k = 0; k < K; ++k) wk[k] = __ldg(p.w + (int64_t)d * K + k);
-        const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
+            for (int k = 0; k < K - 1; ++k) hist[k] = stream_at<T, K>(p, ch, t0 - (K - 1) + k);
+            float wk[K];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t t = (g0 + u) * G;
-            if (t >= L) break;
-            float out[G];
+            for (int k = 0; k < K; ++k) wk[k] = __ldg(p.w + (int64_t)d * K + k);
+            const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
+#pragma unroll 1
+            for (int u = 0; u < U; ++u) {
+                const int64_t t = t0 + u * G;
+                if (t >= L) break;
+                float win[K - 1 + G], out[G];
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                float acc = bias;
+                for (int k = 0; k < K - 1; ++k) win[k] = hist[k];
+                if (VEC && t + G <= L) {
+                    Raw8<T> one;
+                    one.ld(p.x, ch * L + t);
+                    one.get(win + K - 1);
+                } else {
 #pragma unroll
-                for (int k = 0; k < K; ++k) acc = fmaf(wk[k], win[u * G + j + k], acc);
-                out[j] = p.silu ? silu_out<T>(acc) : acc;
-            }
-            if (VEC && t + G <= L) {
-                Vec8<T>::st(p.y, ch * L + t, out);
-            } else {
+                    for (int j = 0; j < G; ++j) win[K - 1 + j] = t + j < L ? Io<T>::ld(p.x, ch * L + t + j) : 0.0f;
+                }
+                conv_vector<T, K>(win, wk, bias, p.silu, out);
+                if (VEC && t + G <= L) {
+                    Vec8<T>::st(p.y, ch * L + t, out);
+                } else {
 #pragma unroll
-                for (int j = 0; j < G; ++j)
-                    if (t + j < L) Io<T>::st(p.y, ch * L + t + j, out[j]);
+                    for (int j = 0; j < G; ++j)
+                        if (t + j < L) Io<T>::st(p.y, ch * L + t + j, out[j]);
+                }
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k) hist[k] = win[G + k];
             }
         }
         if (K > 1 && p.sout && g0 + U >= p.ngroups) {   // the last run: the next segment's history
@@ -164,6 +236,7 @@ __global__ void __launch_bounds__(kThreads) conv_kernel(const ConvArgs p) {
 
 template <typename T, int K>
 cudaError_t launch_k(const ConvArgs &a, bool vec, cudaStream_t st) {
+    constexpr int U = runs_of<T>();
     const int64_t runs = (a.ngroups + U - 1) / U;
     const unsigned bx = (unsigned)(runs >= kThreads ? kThreads : (runs + 31) / 32 * 32);
     const unsigned by = kThreads / bx;
