@@ -143,6 +143,26 @@ def test_start_state_through_checkpoints(variant):
     _compare(g, r, "f32")
 
 
+@pytest.mark.parametrize("L", [1, 31, 32, 33, 64])
+@pytest.mark.parametrize("variant", ["fused", "twopass"])
+def test_chunk_edges(L, variant):
+    """Sequences of one step, one step short of a chunk, exactly one chunk,
+    one step past it, two chunks: the checkpoint count and values, and the
+    backward from them."""
+    p = synth.make_problem(2, 24, 16, L, dtype="f32", gate=True, seed=850 + L, A_mode="random")
+    t = _dev(p)
+    y, fs, ck = _fwd(t, p, variant)
+    torch.cuda.synchronize()
+    ref = _oracle_chunk_states(p, None)
+    assert ck.shape == ((L + CK - 1) // CK, 2, 24, 16)
+    assert_close(ck.cpu().numpy().reshape(ref.shape), ref, "f32", "checkpoints")
+    dy = _dy(p, 25)
+    g = ssm.scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], dy.cuda(), D=t["D"], z=t["z"],
+                     dt_bias=t["dt_bias"], delta_softplus=p.delta_softplus, ckpt=ck)
+    torch.cuda.synchronize()
+    _compare(g, oracle.bwd(*_args(p), dy.float().numpy(), **_kw(p)), "f32")
+
+
 def test_refusals():
     p = synth.make_problem(1, 16, 16, 64, dtype="f32", seed=840)
     t = _dev(p)
