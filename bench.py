@@ -604,6 +604,30 @@ def run_step(args):
     clocks = sampler.stop()
     total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     per = [total_ms / args.steps]
+    # the same layers captured once in a CUDA graph (one token through all of
+    # them) and replayed: the launch-free form of a decode loop
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(copies):
+            layer(i)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(copies):
+            layer(i)
+    replays = max(1, args.steps // copies)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / (replays * copies)
     chans = p.batch * p.dim
     value = world * chans * args.steps / (total_ms / 1e3) / 1e9
     hbm_peak, peak_kind = measured_peaks()
@@ -652,6 +676,10 @@ def run_step(args):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
         "gpu_launches": args.steps,
+        "graph": {"ms_per_step": round(graph_ms, 5),
+                  "achieved_gbs": round(synth.step_min_bytes(p) / (graph_ms / 1e3) / 1e9, 1),
+                  "note": f"the {copies} layers of one token captured once in a CUDA graph and replayed "
+                          f"{replays} times (launch-free decode loop); the line's value is the direct calls"},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
