@@ -22,10 +22,12 @@
  * evaluated the way "Mamba (part 2): parallel scan and hardware-aware
  * optimisation" (scwacadex.pages.dev) sect. 4.2-4.3 describes: the states are
  * never stored for the whole sequence; only the states at the start of every
- * 32-step chunk are computed (by one whole-sequence forward pass that stores
- * them where the channels fill the GPU, else by the two-pass forward's totals
- * pass and carry scan), and each chunk's states are recomputed from its start
- * state while the chunks are walked in reverse.
+ * 32-step chunk are kept -- computed by ssm_scan_bwd (one whole-sequence
+ * forward pass that stores them where the channels fill the GPU, else the
+ * two-pass forward's totals pass and carry scan), or taken from the
+ * checkpoints of the training forward by ssm_scan_bwd_ckpt -- and each
+ * chunk's states are recomputed from its start state while the chunks are
+ * walked in reverse.
  *
  * Layouts as in ssm_scan.h.  dy, dx, ddelta and dz have the forward's I/O
  * dtype and shape [batch, dim, seqlen]; dA [dim, dstate], dB and dC
