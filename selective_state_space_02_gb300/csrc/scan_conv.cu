@@ -143,93 +143,149 @@ __device__ __forceinline__ void conv_vector(const float (&win)[K - 1 + G], const
     }
 }
 
-// Five CTAs of 256 threads per SM (at most 48 registers): the U vectors in
-// flight stay packed, the window of one vector is expanded at a time.
-template <typename T, int K, bool VEC>
-__global__ void __launch_bounds__(kThreads, 5) conv_kernel(const ConvArgs p) {
+// bf16 threads take two channels and issue the next channel's loads before
+// they compute the current one (each thread computes twice the outputs of a
+// float32 thread between its loads); float32 threads take one.
+template <typename T> constexpr int chans_per_thread() { return sizeof(T) == 2 ? 2 : 1; }
+// CTAs per SM the register budget is set for: 4 for the bf16 loop (the
+// current and the next channel's vectors in flight), 5 for float32.
+template <typename T> constexpr int conv_min_blocks() { return sizeof(T) == 2 ? 4 : 5; }
+
+// One run of U vectors of channel ch whose loads are `raw`: the history
+// before it, then window, outputs and store one vector at a time.
+template <typename T, int K>
+__device__ __forceinline__ void conv_whole_run(const ConvArgs &p, int64_t ch, int d, int64_t g0,
+                                               const Raw8<T> (&raw)[runs_of<T>()]) {
     constexpr int U = runs_of<T>();
-    constexpr int KH = K > 1 ? K - 1 : 1;                // the window's history (K - 1 inputs)
+    constexpr int KH = K > 1 ? K - 1 : 1;
+    const int64_t L = p.L, t0 = g0 * G;
+    float hist[KH];                                      // the K-1 inputs before the vector in turn
+    if (K > 1) {
+        if (g0 > 0) {
+            Raw8<T> pv;
+            pv.ld(p.x, ch * L + t0 - G);                 // the neighbouring run's last group: an L1/L2 hit
+            float prev[G];
+            pv.get(prev);
+#pragma unroll
+            for (int k = 0; k < K - 1; ++k) hist[k] = prev[G - (K - 1) + k];
+        } else {
+#pragma unroll
+            for (int k = 0; k < K - 1; ++k) hist[k] = stream_at<T, K>(p, ch, t0 - (K - 1) + k);
+        }
+    }
+    float wk[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) wk[k] = __ldg(p.w + (int64_t)d * K + k);
+    const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        float win[K - 1 + G], out[G];
+#pragma unroll
+        for (int k = 0; k < K - 1; ++k) win[k] = hist[k];
+        raw[u].get(win + K - 1);
+        conv_vector<T, K>(win, wk, bias, p.silu, out);
+        Vec8<T>::st(p.y, ch * L + t0 + u * G, out);
+#pragma unroll
+        for (int k = 0; k < K - 1; ++k) hist[k] = win[G + k];
+    }
+}
+
+// One run of channel ch vector by vector: the row's last run, or rows not
+// 16-byte aligned.
+template <typename T, int K, bool VEC>
+__device__ __forceinline__ void conv_general_run(const ConvArgs &p, int64_t ch, int d, int64_t g0) {
+    constexpr int U = runs_of<T>();
+    constexpr int KH = K > 1 ? K - 1 : 1;
+    const int64_t L = p.L, t0 = g0 * G;
+    float hist[KH];
+#pragma unroll
+    for (int k = 0; k < K - 1; ++k) hist[k] = stream_at<T, K>(p, ch, t0 - (K - 1) + k);
+    float wk[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) wk[k] = __ldg(p.w + (int64_t)d * K + k);
+    const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
+#pragma unroll 1
+    for (int u = 0; u < U; ++u) {
+        const int64_t t = t0 + u * G;
+        if (t >= L) break;
+        float win[K - 1 + G], out[G];
+#pragma unroll
+        for (int k = 0; k < K - 1; ++k) win[k] = hist[k];
+        if (VEC && t + G <= L) {
+            Raw8<T> one;
+            one.ld(p.x, ch * L + t);
+            one.get(win + K - 1);
+        } else {
+#pragma unroll
+            for (int j = 0; j < G; ++j) win[K - 1 + j] = t + j < L ? Io<T>::ld(p.x, ch * L + t + j) : 0.0f;
+        }
+        conv_vector<T, K>(win, wk, bias, p.silu, out);
+        if (VEC && t + G <= L) {
+            Vec8<T>::st(p.y, ch * L + t, out);
+        } else {
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                if (t + j < L) Io<T>::st(p.y, ch * L + t + j, out[j]);
+        }
+#pragma unroll
+        for (int k = 0; k < K - 1; ++k) hist[k] = win[G + k];
+    }
+}
+
+template <typename T, int K, bool VEC>
+__global__ void __launch_bounds__(kThreads, conv_min_blocks<T>()) conv_kernel(const ConvArgs p) {
+    constexpr int U = runs_of<T>();
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // run of U groups
     const int64_t g0 = r * U;
     if (g0 >= p.ngroups) return;                         // no block-wide synchronisation below
     const int64_t L = p.L;
     const int64_t t0 = g0 * G;
-    for (int64_t ch = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; ch < p.nchan;
-         ch += (int64_t)gridDim.y * blockDim.y) {
-        const int d = (int)(ch % p.dim);
-        float hist[KH];                                  // the K-1 inputs before the vector in turn
-        if (VEC && t0 + U * G <= L) {
-            // the whole run inside the row: its U loads first
-            Raw8<T> raw[U];
+    const bool whole = VEC && t0 + U * G <= L;           // the whole run inside the row
+    const int64_t stride = (int64_t)gridDim.y * blockDim.y;
+    int64_t ch = (int64_t)blockIdx.y * blockDim.y + threadIdx.y;
+    if constexpr (chans_per_thread<T>() > 1) {
+        // the next channel's vectors are in flight while the current one is computed
+        Raw8<T> raw[U];
+        if (whole && ch < p.nchan) {
 #pragma unroll
             for (int u = 0; u < U; ++u) raw[u].ld(p.x, ch * L + t0 + u * G);
-            if (K > 1) {
-                if (g0 > 0) {
-                    Raw8<T> pv;
-                    pv.ld(p.x, ch * L + t0 - G);         // the neighbouring run's last group: an L1/L2 hit
-                    float prev[G];
-                    pv.get(prev);
+        }
+        for (; ch < p.nchan; ch += stride) {
+            const int d = (int)(ch % p.dim);
+            if (whole) {
+                Raw8<T> cur[U];
 #pragma unroll
-                    for (int k = 0; k < K - 1; ++k) hist[k] = prev[G - (K - 1) + k];
-                } else {
+                for (int u = 0; u < U; ++u) cur[u] = raw[u];
+                if (ch + stride < p.nchan) {
 #pragma unroll
-                    for (int k = 0; k < K - 1; ++k) hist[k] = stream_at<T, K>(p, ch, t0 - (K - 1) + k);
+                    for (int u = 0; u < U; ++u) raw[u].ld(p.x, (ch + stride) * L + t0 + u * G);
                 }
+                conv_whole_run<T, K>(p, ch, d, g0, cur);
+            } else {
+                conv_general_run<T, K, VEC>(p, ch, d, g0);
             }
-            float wk[K];
+            if (K > 1 && p.sout && g0 + U >= p.ngroups) {   // the last run: the next segment's history
 #pragma unroll
-            for (int k = 0; k < K; ++k) wk[k] = __ldg(p.w + (int64_t)d * K + k);
-            const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float win[K - 1 + G], out[G];
-#pragma unroll
-                for (int k = 0; k < K - 1; ++k) win[k] = hist[k];
-                raw[u].get(win + K - 1);
-                conv_vector<T, K>(win, wk, bias, p.silu, out);
-                Vec8<T>::st(p.y, ch * L + t0 + u * G, out);
-#pragma unroll
-                for (int k = 0; k < K - 1; ++k) hist[k] = win[G + k];
-            }
-        } else {
-            // the row's last run, or rows not 16-byte aligned: one vector at a time
-#pragma unroll
-            for (int k = 0; k < K - 1; ++k) hist[k] = stream_at<T, K>(p, ch, t0 - (K - 1) + k);
-            float wk[K];
-#pragma unroll
-            for (int k = 0; k < K; ++k) wk[k] = __ldg(p.w + (int64_t)d * K + k);
-            const float bias = p.bias ? __ldg(p.bias + d) : 0.0f;
-#pragma unroll 1
-            for (int u = 0; u < U; ++u) {
-                const int64_t t = t0 + u * G;
-                if (t >= L) break;
-                float win[K - 1 + G], out[G];
-#pragma unroll
-                for (int k = 0; k < K - 1; ++k) win[k] = hist[k];
-                if (VEC && t + G <= L) {
-                    Raw8<T> one;
-                    one.ld(p.x, ch * L + t);
-                    one.get(win + K - 1);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < G; ++j) win[K - 1 + j] = t + j < L ? Io<T>::ld(p.x, ch * L + t + j) : 0.0f;
-                }
-                conv_vector<T, K>(win, wk, bias, p.silu, out);
-                if (VEC && t + G <= L) {
-                    Vec8<T>::st(p.y, ch * L + t, out);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < G; ++j)
-                        if (t + j < L) Io<T>::st(p.y, ch * L + t + j, out[j]);
-                }
-#pragma unroll
-                for (int k = 0; k < K - 1; ++k) hist[k] = win[G + k];
+                for (int k = 0; k < K - 1; ++k)
+                    Io<T>::st(p.sout, ch * (K - 1) + k, stream_at<T, K>(p, ch, L - (K - 1) + k));
             }
         }
-        if (K > 1 && p.sout && g0 + U >= p.ngroups) {   // the last run: the next segment's history
+    } else {
+        for (; ch < p.nchan; ch += stride) {
+            const int d = (int)(ch % p.dim);
+            if (whole) {
+                Raw8<T> raw[U];                          // the run's U loads first
 #pragma unroll
-            for (int k = 0; k < K - 1; ++k)
-                Io<T>::st(p.sout, ch * (K - 1) + k, stream_at<T, K>(p, ch, L - (K - 1) + k));
+                for (int u = 0; u < U; ++u) raw[u].ld(p.x, ch * L + t0 + u * G);
+                conv_whole_run<T, K>(p, ch, d, g0, raw);
+            } else {
+                conv_general_run<T, K, VEC>(p, ch, d, g0);
+            }
+            if (K > 1 && p.sout && g0 + U >= p.ngroups) {   // the last run: the next segment's history
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k)
+                    Io<T>::st(p.sout, ch * (K - 1) + k, stream_at<T, K>(p, ch, L - (K - 1) + k));
+            }
         }
     }
 }
@@ -241,7 +297,8 @@ cudaError_t launch_k(const ConvArgs &a, bool vec, cudaStream_t st) {
     const unsigned bx = (unsigned)(runs >= kThreads ? kThreads : (runs + 31) / 32 * 32);
     const unsigned by = kThreads / bx;
     const unsigned gx = (unsigned)((runs + bx - 1) / bx);
-    const int64_t cb = (a.nchan + by - 1) / by;
+    const int64_t per = (int64_t)by * chans_per_thread<T>();
+    const int64_t cb = (a.nchan + per - 1) / per;
     const unsigned gy = (unsigned)(cb < 65535 ? cb : 65535);
     dim3 grid(gx, gy), block(bx, by);
     if (vec) conv_kernel<T, K, true><<<grid, block, 0, st>>>(a);
