@@ -268,20 +268,42 @@ def oracle_full(p):
     return y, fs, time.perf_counter() - t, threads
 
 
+def _single_thread_oracle(p, arrs, budget_s: float = 5.0):
+    """The fp64 oracle on one host thread over a bounded sample of whole
+    channels (every step)."""
+    import numpy as np
+    import oracle
+    nch = p.batch * p.dim
+    probe = list(range(min(nch, 2)))
+    t = time.perf_counter()
+    oracle.fwd(arrs["x"], arrs["delta"], arrs["A"], arrs["B"], arrs["C"], arrs["D"], arrs["z"],
+               arrs["dt_bias"], p.delta_softplus, channels=probe, nthreads=1, return_final_state=False)
+    per_chan = (time.perf_counter() - t) / len(probe)
+    k = int(min(nch, max(len(probe), budget_s / max(per_chan, 1e-9))))
+    chans = list(range(k)) if k == nch else sorted(np.random.default_rng(1).choice(nch, k, replace=False).tolist())
+    t = time.perf_counter()
+    oracle.fwd(arrs["x"], arrs["delta"], arrs["A"], arrs["B"], arrs["C"], arrs["D"], arrs["z"],
+               arrs["dt_bias"], p.delta_softplus, channels=chans, nthreads=1, return_final_state=False)
+    dt = time.perf_counter() - t
+    return {"value": k * p.seqlen / dt / 1e9, "unit": UNIT, "cores": 1,
+            "sample": ("whole workload" if k == nch else f"{k} of {nch} channels") + f", all {p.seqlen} steps ({dt:.2f} s)"}
+
+
 def cpu_baseline(p, max_seconds: float = 20.0, full=None):
     """Time the fp64 oracle on the host cores over a bounded sample of the
-    workload (whole channels, every step).  ``full`` is a finished pass over
-    the whole workload (from the parity check), used when it stayed within the
-    time bound."""
+    workload (whole channels, every step), and on one thread beside it.
+    ``full`` is a finished pass over the whole workload (from the parity
+    check), used when it stayed within the time bound."""
     import numpy as np
     import oracle
     oracle.build()
     nch = p.batch * p.dim
+    arrs = _oracle_arrays(p)
+    one = _single_thread_oracle(p, arrs)
     if full is not None and full[2] <= 1.5 * max_seconds:
         dt, threads = full[2], full[3]
         return {"value": p.elems / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
-                "sample": f"whole workload, all {p.seqlen} steps, one pass ({dt:.2f} s)"}
-    arrs = _oracle_arrays(p)
+                "sample": f"whole workload, all {p.seqlen} steps, one pass ({dt:.2f} s)", "single_thread": one}
     threads = oracle.max_threads()
     # calibrate on a few channels, then size the sample to ~max_seconds / 2
     probe = list(range(min(nch, max(threads, 8))))
@@ -298,7 +320,8 @@ def cpu_baseline(p, max_seconds: float = 20.0, full=None):
     elems = k * p.seqlen
     sample = ("whole workload" if k == nch else f"{k} of {nch} channels") + \
         f", all {p.seqlen} steps, one pass ({dt:.2f} s)"
-    return {"value": elems / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+    return {"value": elems / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+            "single_thread": one}
 
 
 PARITY_TOL = {"f32": 1e-4, "bf16": 2e-2}

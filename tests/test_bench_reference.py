@@ -53,3 +53,16 @@ def test_parity_check_on_cpu():
     y[0, 3, 17] += 1.0
     r = bench.parity_check(p, y, fs, full)
     assert not r["ok"] and r["y_max_scaled_err"] > 2e-2
+
+
+def test_cpu_baseline_reports_one_thread_beside_all_cores():
+    """The bench line's cpu_baseline: the oracle on all host cores over a
+    bounded sample, and on one thread beside it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from selective_state_space_02_gb300 import synth
+    p = synth.make_problem(1, 12, 16, 200, dtype="f32", seed=8)
+    c = bench.cpu_baseline(p, max_seconds=1.0)
+    assert c["kind"] == "oracle" and c["value"] > 0 and c["cores"] >= 1
+    one = c["single_thread"]
+    assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == c["unit"]
