@@ -81,6 +81,8 @@ CASES = [
     (1, 20, 64, 300, "bf16", True, "fused"),      # 64 states: 16-step tiles, a checkpoint every other tile
     (2, 9, 5, 130, "f32", False, "auto"),         # AUTO would run CHUNKED here: TWOPASS instead
     (1, 4880, 16, 100, "f32", True, "auto"),      # AUTO fused at this size
+    (1, 37, 16, 333, "f32", False, "twopass"),    # element loads, segments
+    (1, 20, 32, 300, "bf16", True, "fused"),      # 32 states
 ]
 
 
@@ -107,7 +109,7 @@ def test_checkpoints_match_oracle(case):
     assert_close(ck.cpu().numpy().reshape(ref.shape), ref, "f32", "checkpoints")
 
 
-@pytest.mark.parametrize("case", [CASES[0], CASES[3], CASES[4], CASES[5]], ids=_ids)
+@pytest.mark.parametrize("case", [CASES[0], CASES[3], CASES[4], CASES[5], CASES[7], CASES[8]], ids=_ids)
 def test_backward_from_checkpoints(case):
     b, d, n, L, dt, gate, variant = case
     p = synth.make_problem(b, d, n, L, dtype=dt, gate=gate, seed=820 + d + L, A_mode="random")
