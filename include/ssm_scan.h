@@ -208,8 +208,12 @@ int ssm_scan_fwd_ckpt(const void *x, const void *delta, const float *A, const vo
 
 /* Device status of earlier launches on the current device: bit 0 is set when
  * a kernel's bounded wait on its own TMA copies gave up (the output of that
- * call is then invalid).  Synchronises `stream`; `clear` nonzero resets the
- * word.  Returns the status (>= 0) or SSM_ERR_LAUNCH. */
+ * call is then invalid).  The word is one per device and process, shared by
+ * every call on that device: a set bit says that some call since the last
+ * clear gave up, not which one, so callers that share a device clear and read
+ * it at points where they know which calls ran in between.  Synchronises
+ * `stream`; `clear` nonzero resets the word.  Returns the status (>= 0) or
+ * SSM_ERR_LAUNCH. */
 int ssm_scan_device_status(void *stream, int clear);
 
 /* Self-test of the bounded waits (the failure detection behind
