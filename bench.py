@@ -81,6 +81,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-parity", action="store_true", help="skip the all-element check against the oracle")
     ap.add_argument("--op", default="fwd", choices=["fwd", "step", "bwd", "conv", "convscan"])
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="run the workload's shape with this sequence length instead (smaller cases for profiler "
+                         "captures; the line's config reports it)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -242,10 +245,16 @@ def flush_l2(buf):
     buf.view(-1).max()
 
 
+# --seqlen: the workloads' shapes with another sequence length
+SEQLEN_OVERRIDE = None
+
+
 def workload_problem(name: str, rank: int):
     from selective_state_space_02_gb300 import synth
     cfg = dict(synth.WORKLOADS[name])
     cfg["seed"] = rank_seed(cfg["seed"], rank)
+    if SEQLEN_OVERRIDE:
+        cfg["seqlen"] = SEQLEN_OVERRIDE
     return synth.make_problem(**cfg), cfg
 
 
@@ -412,7 +421,7 @@ def run_ours(args):
     updates = elems * p.dstate
     alu_achieved = updates / kern_s
     alu_peak = alu_peak_updates_per_s()
-    traffic = profiled_traffic(args.workload, variant)
+    traffic = None if SEQLEN_OVERRIDE else profiled_traffic(args.workload, variant)
     roofline = {
         "bound": "alu",
         "achieved": round(alu_achieved / 1e12, 4),
@@ -1089,7 +1098,9 @@ def run_convscan(args):
 
 
 def main(argv=None):
+    global SEQLEN_OVERRIDE
     args = parse_args(argv)
+    SEQLEN_OVERRIDE = args.seqlen
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "step":
