@@ -256,6 +256,8 @@ def scan_step(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torc
     ``state`` [batch, dim, dstate] float32 in place by one token and returns
     y [batch, dim].  x, delta, z: [batch, dim]; B, C: [batch, dstate] (float32
     or bfloat16, all the same); A: [dim, dstate], D, dt_bias: [dim] float32."""
+    # (the checks use the tensors' cheapest attributes: a decode loop calls
+    # this once per layer and token, and the kernel takes about 15 us)
     io = x.dtype
     code = _dtype_code(io)
     for name, t in (("delta", delta), ("B", B), ("C", C), ("z", z)):
@@ -266,7 +268,7 @@ def scan_step(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torc
             raise TypeError(f"{name} must be float32")
     for name, t in (("state", state), ("x", x), ("delta", delta), ("A", A), ("B", B), ("C", C),
                     ("D", D), ("z", z), ("dt_bias", dt_bias)):
-        if t is not None and (not t.is_contiguous() or t.device.type != "cuda"):
+        if t is not None and not (t.is_cuda and t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if x.dim() != 2:
         raise ValueError("x must be [batch, dim]")
@@ -278,9 +280,10 @@ def scan_step(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torc
         raise ValueError("A must be [dim, dstate]; B and C [batch, dstate]")
     if y is None:
         y = torch.empty_like(x)
-    rc = _native.load().ssm_scan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                      _ptr(z), _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), batch, dim,
-                                      N, code, torch.cuda.current_stream(x.device).cuda_stream)
+    lib = _native._lib or _native.load()
+    rc = lib.ssm_scan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                           _ptr(z), _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), batch, dim,
+                           N, code, torch.cuda.current_stream(x.device).cuda_stream)
     _native.check(rc)
     return y
 
