@@ -66,3 +66,20 @@ def test_cpu_baseline_reports_one_thread_beside_all_cores():
     assert c["kind"] == "oracle" and c["value"] > 0 and c["cores"] >= 1
     one = c["single_thread"]
     assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == c["unit"]
+
+
+def test_seqlen_override_for_profiling():
+    """--seqlen runs a workload's shape with another sequence length (smaller
+    profiler captures); the problem and the reported config follow it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args(["--workload", "wide_state_bf16", "--seqlen", "64"])
+    assert args.seqlen == 64
+    old = bench.SEQLEN_OVERRIDE
+    try:
+        bench.SEQLEN_OVERRIDE = 64
+        p, cfg = bench.workload_problem("mid_bf16", 0)
+        assert p.seqlen == 64 and (p.batch, p.dim, p.dstate) == (4, 1536, 16)
+    finally:
+        bench.SEQLEN_OVERRIDE = old
+    assert bench.parse_args([]).seqlen is None
