@@ -618,8 +618,10 @@ scan_kernel(const FwdArgs p, const SegArgs sg, const __grid_constant__ TileMaps 
             // state (Delta/u exchange, B/C loads, a = 2^(Delta A log2 e), u B)
             // for all JB steps, then the JB dependent updates h = a h + u B and
             // the contraction.  The independent half gives the scheduler JB
-            // steps of special-function and load latency to overlap.
-            constexpr int JB = S >= 16 ? 2 : 4;
+            // steps of special-function and load latency to overlap: 8 steps
+            // for narrow lanes of four or more a channel (mid-size shape:
+            // 106.5 -> 104.4 us against 4), 4 for 8 states, 2 for 16 (registers).
+            constexpr int JB = S >= 16 ? 2 : (S <= 4 && NS >= 4) ? 8 : 4;
             float pv[KB];
 #pragma unroll
             for (int j0 = 0; j0 < KB; j0 += JB) {
