@@ -36,6 +36,17 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(t: torch.Tensor) -> int:
+    """The handle of the current CUDA stream on t's device (the cheap lookup
+    where this PyTorch has it: a decode step pays it once per layer and token)."""
+    if _raw_stream is not None:
+        return _raw_stream(t.get_device())
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
 def select_variant(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.float32) -> str:
     v = _native.load().ssm_scan_select_variant(batch, dim, dstate, seqlen, _dtype_code(dtype))
     if v < 0:
@@ -135,7 +146,7 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
         raise ScanError(-2, "invalid sizes or a variant without checkpoints")
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
-    stream = torch.cuda.current_stream(x.device).cuda_stream
+    stream = _stream(x)
     fs = _ptr(final_state) if return_final_state else None
     ws = _ptr(workspace) if ws_bytes else None
     if return_ckpt:
@@ -208,7 +219,7 @@ def scan_fwd_conv(x: torch.Tensor, conv_weight: torch.Tensor, delta: torch.Tenso
         raise ScanError(-8, "this convolution width cannot run fused")
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
-    stream = torch.cuda.current_stream(x.device).cuda_stream
+    stream = _stream(x)
     rc = lib.ssm_scan_fwd_conv(_ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state), width,
                                _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
                                int(bool(delta_softplus)), _ptr(y),
@@ -283,7 +294,7 @@ def scan_step(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torc
     lib = _native._lib or _native.load()
     rc = lib.ssm_scan_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                            _ptr(z), _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), batch, dim,
-                           N, code, torch.cuda.current_stream(x.device).cuda_stream)
+                           N, code, _stream(x))
     _native.check(rc)
     return y
 
@@ -333,7 +344,7 @@ def scan_bwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
                _ptr(dfinal_state), _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
                _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dinitial_state"]),
                batch, dim, N, L, code, _ptr(workspace) if ws_bytes else None, ws_bytes,
-               torch.cuda.current_stream(x.device).cuda_stream)
+               _stream(x))
     _native.check(rc)
     return g
 
@@ -367,6 +378,6 @@ def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] =
         state_out = torch.empty((batch, dim, width - 1), dtype=x.dtype, device=x.device)
     rc = _native.load().ssm_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(state_in), _ptr(y),
                                        _ptr(state_out), int(bool(silu)), batch, dim, L, width, code,
-                                       torch.cuda.current_stream(x.device).cuda_stream)
+                                       _stream(x))
     _native.check(rc)
     return (y, state_out) if return_state else y
